@@ -1,0 +1,364 @@
+"""Benchmark of the window-attention hot path on GB300.
+
+One step = the path between two NaDiT layers on the 720p-area workload
+(T=21, H=45, W=80 -> 75,600 tokens, 24 heads x 128, bf16):
+    regular-layout window attention (gather/scatter through the ids table)
+ -> layout transition regular -> shifted of the hidden state [N, 3072]
+ -> shifted-layout window attention.
+Plans are built once per geometry (as a planner cache would) and timed
+separately.  Inputs are seeded synthetic tensors resident in HBM; each of Q,
+K, V is 464 MB, larger than the 129 MB L2, so no flush is needed between
+steps.
+
+`value` = window-attention FLOPs of both layers / step time (TFLOP/s).
+Prints one JSON line on rank 0.  `--impl reference` times the fp64 CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "window-attention TFLOP/s per step (regular + shifted layer, transition included)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def attn_flops(offsets, heads, d):
+    n = np.diff(np.asarray(offsets, dtype=np.float64))
+    return float(4.0 * np.sum(n * n) * d * heads)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        busy = [s for s in sm if s > 0.5 * (max(smax) if smax else 1)] or sm
+        return {"sm_mhz": float(np.median(busy)) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import shifted_window_attention_gb300 as wsa
+    import wsa_inputs
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = wsa_inputs.WORKLOADS[args.workload]
+    g = (wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw)
+    N, C = wl.num_tokens, wl.channels
+
+    t0 = time.perf_counter()
+    reg = wsa.Plan(*g, wsa.REGULAR)
+    sft = wsa.Plan(*g, wsa.SHIFTED)
+    torch.cuda.synchronize()
+    plan_ms = (time.perf_counter() - t0) * 1e3
+
+    # Inputs: layer 0 (regular) and layer 1 (shifted) Q/K/V, hidden state rows.
+    q0, k0, v0 = wsa_inputs.qkv(wl, layer=0, device=dev)
+    q1, k1, v1 = wsa_inputs.qkv(wl, layer=1, device=dev)
+    x = wsa_inputs.activation(wl, device=dev)
+    o0 = torch.empty_like(q0)
+    o1 = torch.empty_like(q1)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    offs_r = reg.tables()[0].cpu().numpy()
+    offs_s = sft.tables()[0].cpu().numpy()
+    fl_r = attn_flops(offs_r, wl.heads, wl.head_dim)
+    fl_s = attn_flops(offs_s, wl.heads, wl.head_dim)
+    trans_bytes = 2.0 * N * C * 2 + 2 * 4.0 * N  # read + write rows, two int32 table reads
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(i=None):
+        e = ev[i] if i is not None else None
+        if e: e[0].record(stream)
+        wsa.attention(reg, q0, k0, v0, out=o0)
+        if e: e[1].record(stream)
+        wsa.transition(reg, sft, x, out=y)
+        if e: e[2].record(stream)
+        wsa.attention(sft, q1, k1, v1, out=o1)
+        if e: e[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if reg.device_status() or sft.device_status():
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    a_r = [e[0].elapsed_time(e[1]) for e in ev]
+    t_x = [e[1].elapsed_time(e[2]) for e in ev]
+    a_s = [e[2].elapsed_time(e[3]) for e in ev]
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+
+    # End to end through the public API with pinned host buffers: H2D of this
+    # step's Q/K/V (both layers) and hidden rows, the three calls, D2H of the
+    # two attention outputs and the transitioned rows.
+    host_in = [t.cpu().pin_memory() for t in (q0, k0, v0, q1, k1, v1, x)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o0, o1, y)]
+    dev_in = [q0, k0, v0, q1, k1, v1, x]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(1, min(args.steps, 5))
+
+    def e2e_step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        wsa.attention(reg, q0, k0, v0, out=o0)
+        wsa.transition(reg, sft, x, out=y)
+        wsa.attention(sft, q1, k1, v1, out=o1)
+        for h_, d_ in zip(host_out, (o0, o1, y)):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = es.elapsed_time(ee) / e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if reg.device_status() or sft.device_status():
+        raise RuntimeError("device error during the timed region")
+
+    peaks, peak_kind = load_peaks()
+    attn_ms = (np.mean(a_r) + np.mean(a_s)) / 2
+    fl_launch = (fl_r + fl_s) / 2
+    achieved = fl_launch / (attn_ms * 1e-3) / 1e12
+    value = ws * (fl_r + fl_s) / (ms_step * 1e-3) / 1e12
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded torch.randn, N(0,1)/sqrt(2), bf16)",
+        "config": {"workload": f"{wl.name}: T={wl.T},H={wl.H},W={wl.W} ({N} tokens), nt,nh,nw={wl.nt},{wl.nh},{wl.nw} "
+                               f"-> wt,wh,ww={reg.wt},{reg.wh},{reg.ww}; {wl.heads} heads x {wl.head_dim}; "
+                               "regular attn + transition [N,3072] + shifted attn",
+                   "tokens": N, "heads": wl.heads, "head_dim": wl.head_dim,
+                   "windows": [reg.num_windows, sft.num_windows],
+                   "l2": "inputs larger than L2 (Q/K/V 464 MB each); no flush",
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "per_layer": {
+            "attention_ms": [round(float(np.mean(a_r)), 4), round(float(np.mean(a_s)), 4)],
+            "attention_tflops": [round(fl_r / (np.mean(a_r) * 1e9), 1), round(fl_s / (np.mean(a_s) * 1e9), 1)],
+            "tokens_per_s": [round(N / (np.mean(a_r) * 1e-3)), round(N / (np.mean(a_s) * 1e-3))],
+            "transition_ms": round(float(np.mean(t_x)), 4),
+            "transition_gbs": round(trans_bytes / (np.mean(t_x) * 1e6), 1),
+            "transition_frac_hbm": round(trans_bytes / (np.mean(t_x) * 1e6) / peaks["hbm_gbs"], 4),
+            "plan_build_ms_host_incl": round(plan_ms, 3),
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "attention_tc_kernel",
+            "achieved": round(achieved, 2),
+            "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+            "peak_source": f"{peak_kind} bf16 burst",
+            "traffic": None,
+        },
+        "e2e": {"value": round(ws * (fl_r + fl_s) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, tuple(t.float().cpu().numpy() for t in (q0, k0, v0)),
+                                              seconds=args.cpu_seconds)
+    if ws > 1:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def cpu_inputs(wl):
+    """The workload's layer-0 Q/K/V as fp32 numpy arrays (drawn on the GPU when
+    one is present, which is faster; the CPU draw otherwise)."""
+    import torch
+    import wsa_inputs
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    return tuple(t.float().cpu().numpy() for t in wsa_inputs.qkv(wl, layer=0, device=dev))
+
+
+def cpu_baseline(wl, inputs, seconds=15.0, layout=0, seed=0):
+    """Time the fp64 oracle as it stands on a bounded sample of the workload:
+    whole (window, head) problems of one layout, in seeded order, through
+    oracle.window_attention_rows, until `seconds` of CPU work are done.
+    Returns TFLOP/s of algorithmic attention work."""
+    import oracle
+
+    q, k, v = inputs
+    g = (wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw)
+    p = oracle.make_plan(*g, layout)
+    rng = np.random.default_rng(seed)
+    order = [(int(w), int(h)) for w in rng.permutation(p.num_windows) for h in rng.permutation(wl.heads)]
+    flops, done, t_total = 0.0, 0, 0.0
+    for (w, h) in order:
+        n = int(p.offsets[w + 1] - p.offsets[w])
+        t0 = time.perf_counter()
+        oracle.window_attention_rows(q, k, v, p, w, h, np.arange(n))
+        t_total += time.perf_counter() - t0
+        flops += 4.0 * n * n * wl.head_dim
+        done += 1
+        if t_total >= seconds:
+            break
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count()
+    return {"value": round(flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} whole (window, head) problems of the {wl.name} "
+                      f"{'regular' if layout == 0 else 'shifted'} layer, fp64 numpy, {t_total:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import wsa_inputs
+    wl = wsa_inputs.WORKLOADS[args.workload]
+    inputs = cpu_inputs(wl)
+    vals = []
+    per = max(2.0, 90.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(wl, inputs, seconds=per, layout=i % 2, seed=i)
+        if i >= args.warmup:
+            vals.append(r)
+    value = float(np.mean([r["value"] for r in vals]))
+    cores = vals[0]["cores"]
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {vals[0]['sample']}"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="720p")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

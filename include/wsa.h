@@ -1,0 +1,156 @@
+/*
+ * wsa.h -- C ABI of the GB300 (sm_103a) window-attention library.
+ *
+ * NaDiT-style 3D window attention over a post-patch video token grid
+ * (T, H, W) with alternating regular and shifted window layouts, as described
+ * in the vllm-omni design note "Window-Aligned Sequence Parallelism (SeedVR2)".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Plain C types only.  Device pointers are CUDA device addresses on the
+ *   current device; host pointers are ordinary host memory.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every device call is asynchronous on that stream.
+ * - The caller owns every tensor it passes.  A plan owns its device tables
+ *   until wsa_plan_destroy().
+ * - Argument errors are detected on the host before anything is launched; an
+ *   argument error never leaves a partially written output.
+ * - On failure a call returns a negative wsa_status and records a message that
+ *   wsa_last_error() returns (per host thread).
+ * - Non-finite inputs are not validated: they propagate as IEEE arithmetic
+ *   does.
+ */
+#ifndef WSA_H_
+#define WSA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct wsa_plan_s* wsa_plan_t; /* opaque; owned by the library */
+
+typedef enum {
+  WSA_OK = 0,
+  WSA_ERR_INVALID_ARG = -1,  /* bad size, null pointer, misalignment */
+  WSA_ERR_UNSUPPORTED = -2,  /* valid request this library does not implement */
+  WSA_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
+  WSA_ERR_OOM = -4,          /* device allocation failed */
+  WSA_ERR_MISMATCH = -5,     /* plans of different grids */
+  WSA_ERR_DEVICE_CHECK = -6  /* a kernel recorded an error word (see wsa_plan_device_status) */
+} wsa_status;
+
+typedef enum { WSA_BF16 = 0, WSA_FP32 = 1 } wsa_dtype;
+typedef enum { WSA_REGULAR = 0, WSA_SHIFTED = 1 } wsa_layout;
+
+/* Library ABI version (major*100 + minor). */
+int wsa_version(void);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* wsa_last_error(void);
+
+/*
+ * wsa_window_size -- host only, needs no GPU.
+ * Window size of "Window layouts": scale = sqrt(45*80/(H*W)),
+ * wh = ceil(round(H*scale)/nh), ww = ceil(round(W*scale)/nw),
+ * wt = ceil(min(T, max_temporal)/nt), round = round-half-to-even in fp64.
+ * All of T,H,W,nt,nh,nw,max_temporal must be > 0 (max_temporal is 30 in the
+ * note); a size that computes to 0 is WSA_ERR_INVALID_ARG.
+ */
+wsa_status wsa_window_size(int T, int H, int W, int nt, int nh, int nw,
+                           int max_temporal, int* wt, int* wh, int* ww);
+
+/*
+ * wsa_layout_windows -- host only, needs no GPU.
+ * Windows of one layout ("Window layouts": regular cuts at multiples of the
+ * window size, shifted cuts moved by floor(w/2) and clipped to the grid, no
+ * cyclic roll; an axis not longer than its window is not shifted; empty
+ * intervals are dropped), enumerated w-outermost, t-innermost.
+ * Writes *num_windows always; if dims != NULL and capacity >= *num_windows,
+ * also writes dims[6*k .. 6*k+5] = (t0, t1, h0, h1, w0, w1) of window k
+ * (half-open).  capacity too small with dims != NULL is WSA_ERR_INVALID_ARG.
+ */
+wsa_status wsa_layout_windows(int T, int H, int W, int nt, int nh, int nw,
+                              wsa_layout layout, int max_temporal,
+                              int* dims, int capacity, int* num_windows);
+
+/*
+ * wsa_plan_create -- builds one layout's plan on the current device.
+ * Host: window size and cuts (as wsa_layout_windows), ragged window offsets
+ * in the cu_seqlens convention (vLLM-Omni diffusion-runtime blog, section
+ * 4.2: prefix sums from 0 to N), and the attention work lists.  Device: a
+ * kernel writes ids[p] = canonical id (t*H + h)*W + w of packed position p
+ * (windows in enumeration order, tokens row-major in (t, h, w) inside a
+ * window -- "Window layouts") and pos[ids[p]] = p.
+ * N = T*H*W must be < 2^31.  The plan allocates its tables with cudaMalloc
+ * (synchronous); they are filled asynchronously on `stream`.
+ */
+wsa_status wsa_plan_create(int T, int H, int W, int nt, int nh, int nw,
+                           wsa_layout layout, int max_temporal, void* stream,
+                           wsa_plan_t* out);
+
+/* Frees the plan and its device tables (cudaFree: synchronises the device). */
+wsa_status wsa_plan_destroy(wsa_plan_t plan);
+
+/* Sizes of a plan.  Any output pointer may be NULL. */
+wsa_status wsa_plan_info(wsa_plan_t plan, int* num_windows, int* num_tokens,
+                         int* max_window_tokens, int* wt, int* wh, int* ww,
+                         int* layout);
+
+/*
+ * Device pointers to the plan's int32 tables, valid until wsa_plan_destroy:
+ *   offsets [num_windows + 1], dims [num_windows * 6], ids [N], pos [N].
+ * Read-only for the caller.  Any output pointer may be NULL.
+ */
+wsa_status wsa_plan_tables(wsa_plan_t plan, const int** offsets, const int** dims,
+                           const int** ids, const int** pos);
+
+/*
+ * wsa_attention -- per-window softmax attention over all heads.
+ * "Window-Aligned Sequence Parallelism (SeedVR2)", section "Motivation":
+ * attention runs only inside each window; for window w and head h
+ *     O[w,h] = softmax(Q[w,h] K[w,h]^T * softmax_scale) V[w,h]
+ * with no mask inside a window and no term across windows.
+ *
+ * q, k, v, o: device, [N, heads, head_dim] contiguous (token-major, heads,
+ *   then channels).  in_order_canonical = 1: row = canonical token id;
+ *   0: row = packed position of the plan (what wsa_transition produces).
+ *   The window gather and the output scatter go through the plan's ids table
+ *   inside the kernel; no separate permutation pass runs.
+ * dtype WSA_BF16: head_dim must be 128; tensor-core kernel (tcgen05, TMEM),
+ *   fp32 accumulation and softmax, bf16 output; pointers 16-byte aligned.
+ * dtype WSA_FP32: head_dim 64 or 128; fp32 CUDA-core kernel throughout.
+ * softmax_scale <= 0 selects 1/sqrt(head_dim).
+ * o must not alias q, k or v.  Calls that use the same plan must be ordered
+ * on one stream (the plan holds the kernel's work counter).
+ */
+wsa_status wsa_attention(wsa_plan_t plan, const void* q, const void* k,
+                         const void* v, void* o, int heads, int head_dim,
+                         wsa_dtype dtype, int in_order_canonical,
+                         float softmax_scale, void* stream);
+
+/*
+ * wsa_transition -- the local-permutation layout change between layers.
+ * "Window-Aligned Sequence Parallelism (SeedVR2)", sections "Motivation" and
+ * "Plan A redistribution": with one rank a layout change is a permutation of
+ * the activation rows.  x_src holds row p = token at packed position p of
+ * `src`; x_dst receives row p = token at packed position p of `dst`, i.e.
+ *     x_dst[p] = x_src[pos_src[ids_dst[p]]].
+ * x_src, x_dst: device, [N, channels] contiguous of `dtype`, must not
+ * overlap.  src and dst may be the same plan (plain copy).  Plans of
+ * different grids: WSA_ERR_MISMATCH.  Bit-exact (pure data movement).
+ */
+wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src,
+                          void* x_dst, int channels, wsa_dtype dtype, void* stream);
+
+/*
+ * Reads and clears the plan's device error word (synchronises the device).
+ * *code = 0 when no kernel recorded an error; otherwise the code of the first
+ * bounded wait that gave up, and the call returns WSA_ERR_DEVICE_CHECK.
+ */
+wsa_status wsa_plan_device_status(wsa_plan_t plan, int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WSA_H_ */

@@ -1,0 +1,213 @@
+"""Python binding of libwsa.so: GB300 NaDiT-style 3D window attention.
+
+Thin ctypes marshalling over the C ABI declared in ``include/wsa.h``: every
+function below converts torch tensors to device pointers, passes the current
+CUDA stream and raises on a non-zero status.  All computation happens in the
+library's CUDA kernels; there is no CPU path.  Importing this package fails
+loudly when the library has not been built (``__graft_entry__.build()`` or
+``python shifted_window_attention_gb300/_build.py``).
+"""
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libwsa.so")
+
+REGULAR = 0
+SHIFTED = 1
+BF16 = 0
+FP32 = 1
+
+_STATUS = {
+    0: "WSA_OK",
+    -1: "WSA_ERR_INVALID_ARG",
+    -2: "WSA_ERR_UNSUPPORTED",
+    -3: "WSA_ERR_CUDA",
+    -4: "WSA_ERR_OOM",
+    -5: "WSA_ERR_MISMATCH",
+    -6: "WSA_ERR_DEVICE_CHECK",
+}
+
+
+class WsaError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.name = _STATUS.get(status, str(status))
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    i, p, f = ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+    ip = ctypes.POINTER(ctypes.c_int)
+    sigs = {
+        "wsa_version": ([], i),
+        "wsa_last_error": ([], ctypes.c_char_p),
+        "wsa_window_size": ([i] * 7 + [ip] * 3, i),
+        "wsa_layout_windows": ([i] * 8 + [ip, i, ip], i),
+        "wsa_plan_create": ([i] * 8 + [p, ctypes.POINTER(p)], i),
+        "wsa_plan_destroy": ([p], i),
+        "wsa_plan_info": ([p] + [ip] * 7, i),
+        "wsa_plan_tables": ([p] + [ctypes.POINTER(p)] * 4, i),
+        "wsa_attention": ([p, p, p, p, p, i, i, i, i, f, p], i),
+        "wsa_transition": ([p, p, p, p, i, i, p], i),
+        "wsa_plan_device_status": ([p, ip], i),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+lib = _load()
+
+
+def _check(status):
+    if status != 0:
+        raise WsaError(status, lib.wsa_last_error().decode())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def version():
+    return lib.wsa_version()
+
+
+def window_size(T, H, W, nt, nh, nw, max_temporal=30):
+    """Host-only: (wt, wh, ww) of the window note's formula."""
+    out = [ctypes.c_int() for _ in range(3)]
+    _check(lib.wsa_window_size(T, H, W, nt, nh, nw, max_temporal, *[ctypes.byref(o) for o in out]))
+    return tuple(o.value for o in out)
+
+
+def layout_windows(T, H, W, nt, nh, nw, layout, max_temporal=30):
+    """Host-only: list of (t0, t1, h0, h1, w0, w1) in enumeration order."""
+    n = ctypes.c_int()
+    _check(lib.wsa_layout_windows(T, H, W, nt, nh, nw, layout, max_temporal, None, 0, ctypes.byref(n)))
+    buf = (ctypes.c_int * (6 * n.value))()
+    _check(lib.wsa_layout_windows(T, H, W, nt, nh, nw, layout, max_temporal, buf, n.value, ctypes.byref(n)))
+    return [tuple(buf[6 * k:6 * k + 6]) for k in range(n.value)]
+
+
+class _DeviceArray:
+    """Zero-copy view of a library-owned int32 device table."""
+
+    def __init__(self, ptr, n, owner):
+        self._owner = owner  # keeps the plan alive while the view exists
+        self.__cuda_array_interface__ = {
+            "shape": (n,), "typestr": "<i4", "data": (ptr, True), "version": 3, "strides": None,
+        }
+
+
+class Plan:
+    """One layout's window plan on the current CUDA device (wsa_plan_create)."""
+
+    def __init__(self, T, H, W, nt, nh, nw, layout, max_temporal=30, stream=None):
+        h = ctypes.c_void_p()
+        _check(lib.wsa_plan_create(T, H, W, nt, nh, nw, layout, max_temporal, _stream(stream),
+                                   ctypes.byref(h)))
+        self._h = h
+        self.T, self.H, self.W = T, H, W
+        vals = [ctypes.c_int() for _ in range(7)]
+        _check(lib.wsa_plan_info(h, *[ctypes.byref(v) for v in vals]))
+        (self.num_windows, self.num_tokens, self.max_window_tokens,
+         self.wt, self.wh, self.ww, self.layout) = (v.value for v in vals)
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise WsaError(-1, "plan was destroyed")
+        return self._h
+
+    def tables(self):
+        """(offsets, dims, ids, pos) as int32 CUDA tensors sharing the plan's memory."""
+        ptrs = [ctypes.c_void_p() for _ in range(4)]
+        _check(lib.wsa_plan_tables(self.handle, *[ctypes.byref(x) for x in ptrs]))
+        sizes = [self.num_windows + 1, 6 * self.num_windows, self.num_tokens, self.num_tokens]
+        dev = torch.device("cuda", torch.cuda.current_device())
+        return tuple(torch.as_tensor(_DeviceArray(x.value, n, self), device=dev)
+                     for x, n in zip(ptrs, sizes))
+
+    def device_status(self):
+        """Synchronises; returns 0 or raises WsaError with the recorded device code."""
+        code = ctypes.c_int()
+        st = lib.wsa_plan_device_status(self.handle, ctypes.byref(code))
+        _check(st)
+        return code.value
+
+    def destroy(self):
+        if self._h is not None:
+            _check(lib.wsa_plan_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            if self._h is not None and lib is not None:
+                lib.wsa_plan_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise WsaError(-2, f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attention(plan, q, k, v, out=None, canonical=True, scale=0.0, stream=None):
+    """Per-window softmax(Q K^T * scale) V for all heads.
+
+    q, k, v: CUDA tensors [N, heads, head_dim], contiguous, same dtype (bf16 or
+    fp32).  canonical=True: row = canonical token id; False: row = packed
+    position of ``plan``.  Returns ``out`` (allocated if None)."""
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise WsaError(-1, "q, k, v must be contiguous 3-D CUDA tensors")
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise WsaError(-1, "q, k, v must share shape and dtype")
+    if q.shape[0] != plan.num_tokens:
+        raise WsaError(-1, f"q has {q.shape[0]} rows, the plan has {plan.num_tokens} tokens")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise WsaError(-1, "out must match q")
+    _check(lib.wsa_attention(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), q.shape[1], q.shape[2],
+                             _dtype_code(q), 1 if canonical else 0, float(scale), _stream(stream)))
+    return out
+
+
+def transition(src, dst, x, out=None, stream=None):
+    """Rows of x (packed order of plan ``src``) rearranged into the packed order
+    of plan ``dst``: out[p] = x[pos_src[ids_dst[p]]]."""
+    if not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
+        raise WsaError(-1, "x must be a contiguous 2-D CUDA tensor")
+    if x.shape[0] != src.num_tokens:
+        raise WsaError(-1, "x row count does not match the plan")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise WsaError(-1, "out must match x")
+    _check(lib.wsa_transition(src.handle, dst.handle, _ptr(x), _ptr(out), x.shape[1], _dtype_code(x),
+                              _stream(stream)))
+    return out
+
+
+__all__ = [
+    "REGULAR", "SHIFTED", "BF16", "FP32", "WsaError", "Plan", "attention", "transition",
+    "window_size", "layout_windows", "version", "lib",
+]

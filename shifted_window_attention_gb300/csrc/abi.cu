@@ -1,0 +1,91 @@
+// C-ABI entry points for attention and the layout transition: argument
+// validation on the host, then one kernel launch each.  Each dtype has exactly
+// one kernel; nothing falls back to another implementation.
+
+#include <cmath>
+#include <cstdint>
+
+#include "wsa_internal.h"
+
+using namespace wsa;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const auto x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+wsa_status wsa_attention(wsa_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                         int heads, int head_dim, wsa_dtype dtype, int in_order_canonical,
+                         float softmax_scale, void* stream) {
+  if (!plan) return fail(WSA_ERR_INVALID_ARG, "plan is null");
+  if (!q || !k || !v || !o) return fail(WSA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (heads <= 0) return fail(WSA_ERR_INVALID_ARG, "heads must be > 0");
+  if (dtype != WSA_BF16 && dtype != WSA_FP32) return fail(WSA_ERR_INVALID_ARG, "unknown dtype");
+  if (in_order_canonical != 0 && in_order_canonical != 1)
+    return fail(WSA_ERR_INVALID_ARG, "in_order_canonical must be 0 or 1");
+  if (!std::isfinite(softmax_scale)) return fail(WSA_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (dtype == WSA_BF16 && head_dim != 128)
+    return fail(WSA_ERR_UNSUPPORTED, "bf16 attention supports head_dim 128 only");
+  if (dtype == WSA_FP32 && head_dim != 64 && head_dim != 128)
+    return fail(WSA_ERR_UNSUPPORTED, "fp32 attention supports head_dim 64 or 128");
+  const size_t elt = dtype == WSA_BF16 ? 2 : 4;
+  const size_t bytes = static_cast<size_t>(plan->num_tokens) * heads * head_dim * elt;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(WSA_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (overlap(o, bytes, q, bytes) || overlap(o, bytes, k, bytes) || overlap(o, bytes, v, bytes))
+    return fail(WSA_ERR_INVALID_ARG, "o must not overlap q, k or v");
+  if (static_cast<long long>(plan->num_tc_items) * heads >= (1LL << 31))
+    return fail(WSA_ERR_UNSUPPORTED, "too many work units (windows x heads)");
+  if (heads > 65535 && dtype == WSA_FP32)
+    return fail(WSA_ERR_UNSUPPORTED, "fp32 attention supports at most 65535 heads");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_attention: cudaGetDevice");
+  if (dev != plan->device) return fail(WSA_ERR_INVALID_ARG, "plan was created on another device");
+
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == WSA_FP32) {
+    e = launch_attention_fp32(*plan, static_cast<const float*>(q), static_cast<const float*>(k),
+                              static_cast<const float*>(v), static_cast<float*>(o), heads, head_dim,
+                              in_order_canonical == 1, scale, s);
+  } else {
+    e = launch_attention_bf16_tc(*plan, q, k, v, o, heads, in_order_canonical == 1, scale, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_attention: launch");
+  return WSA_OK;
+}
+
+wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src, void* x_dst, int channels,
+                          wsa_dtype dtype, void* stream) {
+  if (!src || !dst) return fail(WSA_ERR_INVALID_ARG, "plans must be non-null");
+  if (!x_src || !x_dst) return fail(WSA_ERR_INVALID_ARG, "x_src and x_dst must be non-null");
+  if (channels <= 0) return fail(WSA_ERR_INVALID_ARG, "channels must be > 0");
+  if (dtype != WSA_BF16 && dtype != WSA_FP32) return fail(WSA_ERR_INVALID_ARG, "unknown dtype");
+  if (src->T != dst->T || src->H != dst->H || src->W != dst->W)
+    return fail(WSA_ERR_MISMATCH, "plans describe different grids");
+  if (src->device != dst->device) return fail(WSA_ERR_INVALID_ARG, "plans live on different devices");
+  const size_t elt = dtype == WSA_BF16 ? 2 : 4;
+  const size_t row_bytes = static_cast<size_t>(channels) * elt;
+  const size_t bytes = row_bytes * static_cast<size_t>(src->num_tokens);
+  if (reinterpret_cast<uintptr_t>(x_src) % elt || reinterpret_cast<uintptr_t>(x_dst) % elt)
+    return fail(WSA_ERR_INVALID_ARG, "x_src and x_dst must be aligned to the element size");
+  if (overlap(x_src, bytes, x_dst, bytes)) return fail(WSA_ERR_INVALID_ARG, "x_src and x_dst overlap");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_transition: cudaGetDevice");
+  if (dev != src->device) return fail(WSA_ERR_INVALID_ARG, "plans were created on another device");
+  e = launch_transition(*src, *dst, x_src, x_dst, row_bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_transition: launch");
+  return WSA_OK;
+}
+
+}  // extern "C"

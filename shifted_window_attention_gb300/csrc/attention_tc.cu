@@ -1,0 +1,667 @@
+// Tensor-core window attention for sm_103a: bf16 Q/K/V, fp32 accumulation and
+// softmax, bf16 output.
+//
+// What it computes ("Window-Aligned Sequence Parallelism (SeedVR2)", section
+// "Motivation"): for every window w of a plan and every head h,
+//     O[w,h] = softmax(Q[w,h] K[w,h]^T * scale) V[w,h],
+// attention only inside the window.  Rows of a window are gathered from the
+// token-major [N, heads, 128] tensors through the plan's ids table and the
+// output rows are scattered back through it, so no separate permutation pass
+// touches HBM.
+//
+// Design (Blackwell, one CTA per SM, persistent):
+//  * A work unit is (window, head, 256 query rows) -- two 128-row Q tiles that
+//    share every K/V tile, halving K/V traffic per FLOP.  Units are handed out
+//    by an atomic counter in heaviest-first order (the note's LPT rule applied
+//    to kernel work units), so ragged edge windows fill the tail.
+//  * Warp roles: warps 0-3 run the softmax of Q tile 0 and warps 4-7 that of
+//    Q tile 1 (one query row per thread = one TMEM lane); warps 8-11 gather
+//    Q/K/V rows with 16-byte cp.async into 128B-swizzled shared-memory tiles;
+//    one thread of warp 12 issues every tcgen05.mma.
+//  * TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The bf16
+//    probabilities P overwrite the first 64 columns of their S tile and feed
+//    the P V product straight from TMEM (A operand in TMEM); V is the B
+//    operand, read MN-major from shared memory.
+//  * Online softmax in the log2 domain with a lazy rescale: the running max is
+//    only raised (and O rescaled in TMEM) when a row's max grows by more than
+//    2^8, which keeps every probability <= 256 and the result exact up to
+//    rounding.
+//  * Every wait is bounded: after ~1 s a wait records an error code in the
+//    plan's workspace and the CTA unwinds, drains its MMAs and cp.asyncs and
+//    frees TMEM.
+
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "wsa_internal.h"
+
+namespace wsa {
+namespace {
+
+constexpr int kD = 128;                     // head dim
+constexpr int kTile = 128;                  // rows of a Q / K / V tile
+constexpr int kTileBytes = kTile * kD * 2;  // 32 KB
+constexpr int kPanelBytes = kTile * 128;    // 128 rows x 128 B (64 channels), one swizzle panel
+constexpr int kSlots = 4;                   // K/V ring slots
+constexpr int kLoaderWarp0 = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 13 * 32;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+
+enum : int {
+  B_RING_FULL = 0,
+  B_RING_EMPTY = B_RING_FULL + kSlots,
+  B_Q_FULL = B_RING_EMPTY + kSlots,
+  B_Q_EMPTY,
+  B_S_FULL,                    // 2
+  B_P_FULL = B_S_FULL + 2,     // 2
+  B_O_FULL = B_P_FULL + 2,     // 2
+  B_UNIT_FULL = B_O_FULL + 2,  // 2
+  B_UNIT_EMPTY = B_UNIT_FULL + 2,
+  B_DRAIN = B_UNIT_EMPTY + 2,
+  B_COUNT
+};
+
+constexpr int kSmemQ = 0;                                   // Q0 | Q1
+constexpr int kSmemRing = 2 * kTileBytes;                   // kSlots K/V tiles
+constexpr int kSmemBars = kSmemRing + kSlots * kTileBytes;  // mbarriers
+constexpr int kSmemUnits = kSmemBars + ((8 * B_COUNT + 15) / 16) * 16;
+constexpr int kSmemTmem = kSmemUnits + 2 * 16;
+constexpr int kSmemUsed = kSmemTmem + 16;
+constexpr int kSmemAlloc = kSmemUsed + 1024;  // slack for 1 KB alignment of the tiles
+
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+constexpr uint32_t kTmemCols = 512;
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
+// B bf16 (10-12 = 1), A K-major (bit 15 = 0), N>>3 at bits 17-22, M>>4 at 24-28.
+constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// P V: B (= V) is MN-major (bit 16).
+constexpr uint32_t kIdescPV = kIdescS | (1u << 16);
+
+// Error codes recorded in the workspace error word (which wait gave up).
+enum : int {
+  E_LOAD_UNIT_EMPTY = 0x101, E_LOAD_UNIT_FULL, E_LOAD_Q_EMPTY, E_LOAD_RING_EMPTY,
+  E_MMA_UNIT_FULL = 0x201, E_MMA_Q_FULL, E_MMA_K_FULL, E_MMA_V_FULL, E_MMA_P0, E_MMA_P1, E_MMA_DRAIN,
+  E_SM_UNIT_FULL = 0x301, E_SM_S_FULL, E_SM_O_FULL
+};
+
+struct TcParams {
+  const char* q;
+  const char* k;
+  const char* v;
+  char* o;
+  const int* row_map;  // ids table (canonical order) or nullptr (packed order)
+  const int* offsets;
+  const WorkItem* items;
+  int num_units;
+  int heads;
+  long long row_stride;  // bytes between consecutive tokens (heads * 256)
+  float c;               // softmax scale * log2(e)
+  int* work;             // workspace words
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Gives up when another thread has
+// recorded an error, or after kWaitCycles, recording `code` first.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* err, int code) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*reinterpret_cast<volatile int*>(err) != 0) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        atomicCAS(err, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// Makes this thread's completed generic-proxy shared-memory writes visible to
+// the async proxy (the tensor core reads its operands through it).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Arrives on `bar` once every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// D(tmem) (+)= A(tmem) * B(smem)
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading/stride byte offsets
+// (16-byte units), version 1 (bits 46-47), 128-byte swizzle (bits 61-63 = 2).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// K-major operand (Q or K tile, 128 rows x 128 channels): K-step kk covers
+// channels 16kk..16kk+15: panel kk/4, 32-byte offset (kk%4) inside the
+// swizzled 128-byte row; 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+  return smem_desc(tile + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+}
+
+// MN-major B operand (V tile: K = key rows, N = channels): K-step kk covers
+// key rows 16kk..16kk+15 (two 8-row groups 1024 bytes apart); the two
+// 64-channel panels are kPanelBytes apart.
+__device__ __forceinline__ uint64_t desc_v(uint32_t tile, int kk) {
+  return smem_desc(tile + kk * 2048, kPanelBytes, 1024);
+}
+
+#define WSA_R8(b) "=r"(r[b]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), "=r"(r[b + 5]), \
+                  "=r"(r[b + 6]), "=r"(r[b + 7])
+#define WSA_W8(b) "r"(r[b]), "r"(r[b + 1]), "r"(r[b + 2]), "r"(r[b + 3]), "r"(r[b + 4]), "r"(r[b + 5]), \
+                  "r"(r[b + 6]), "r"(r[b + 7])
+
+// 64 consecutive fp32 columns of this thread's TMEM lane; the wait is inside
+// the same asm statement so no use of the registers can be scheduled before it.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,"
+      "%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,"
+      "%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : WSA_R8(0), WSA_R8(8), WSA_R8(16), WSA_R8(24), WSA_R8(32), WSA_R8(40), WSA_R8(48), WSA_R8(56)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,"
+      "%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      WSA_W8(0), WSA_W8(8), WSA_W8(16), WSA_W8(24)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------- roles
+
+struct Smem {
+  uint32_t q0, ring, bars;
+  int4* units;
+};
+
+__device__ __forceinline__ uint32_t bar_at(const Smem& s, int i) { return s.bars + 8u * static_cast<uint32_t>(i); }
+
+// Gather warps (4): rows 32*lw .. 32*lw+31 of every tile.  A half-warp copies
+// one 256-byte row (16 chunks of 16 bytes), so each lane issues 16 cp.async
+// per tile.  Shared layout: two 64-channel panels of 128 rows x 128 bytes,
+// chunk c of row r stored at chunk position c ^ (r % 8) (128-byte swizzle).
+__device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm, int lw, int lane) {
+  int* err = prm.work + WS_ERROR;
+  const int half = lane >> 4;
+  const int chunk = lane & 15;
+  const uint32_t panel_off = static_cast<uint32_t>((chunk >> 3) * kPanelBytes);
+  const int cc = chunk & 7;
+  uint32_t ring_iter = 0, unit_iter = 0;
+  uint32_t pending = 0;
+  bool has_pending = false;  // warp-uniform
+
+  auto flush = [&]() {
+    if (has_pending) {
+      cp_async_wait_all();
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pending);
+      has_pending = false;
+    }
+  };
+  // Closes the copy group just issued; signals the previous group once it landed.
+  auto rotate = [&](uint32_t full_bar) {
+    cp_async_commit();
+    if (has_pending) {
+      cp_async_wait_1();
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pending);
+    }
+    pending = full_bar;
+    has_pending = true;
+  };
+  // Never blocks while a finished-but-unsignalled copy group is held back.
+  auto acquire = [&](uint32_t bar, uint32_t parity, int code) -> bool {
+    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+    flush();
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, err, code));
+  };
+  auto load_tile = [&](const char* src, uint32_t dst, int row0, int n, int off, int head) {
+    const int myrow = row0 + 32 * lw + lane;
+    int myid = -1;
+    if (myrow < n) myid = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+    const char* colbase = src + static_cast<long long>(head) * (kD * 2) + chunk * 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int r = 32 * lw + half + 2 * i;
+      const int id = __shfl_sync(0xffffffffu, myid, half + 2 * i);
+      const char* g = id >= 0 ? colbase + static_cast<long long>(id) * prm.row_stride : src;
+      cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
+    }
+  };
+  auto load_kv = [&](int j, int n, int off, int head) -> bool {
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t slot = ring_iter % kSlots;
+      if (!acquire(bar_at(sm, B_RING_EMPTY + slot), ((ring_iter / kSlots) & 1) ^ 1, E_LOAD_RING_EMPTY))
+        return false;
+      load_tile(which ? prm.v : prm.k, sm.ring + slot * kTileBytes, j * kTile, n, off, head);
+      rotate(bar_at(sm, B_RING_FULL + slot));
+      ++ring_iter;
+    }
+    return true;
+  };
+
+  while (true) {
+    const int us = unit_iter & 1;
+    const uint32_t uph = (unit_iter >> 1) & 1;
+    if (lw == 0) {
+      // The first gather warp hands out the next unit to every role.
+      if (!acquire(bar_at(sm, B_UNIT_EMPTY + us), uph ^ 1, E_LOAD_UNIT_EMPTY)) break;
+      if (lane == 0) {
+        const int u = atomicAdd(prm.work + WS_NEXT_UNIT, 1);
+        int4 info = make_int4(0, -1, 0, 0);
+        if (u < prm.num_units) {
+          const WorkItem it = prm.items[u / prm.heads];
+          const int off = prm.offsets[it.window];
+          info = make_int4(off, prm.offsets[it.window + 1] - off, it.q_start, u % prm.heads);
+        }
+        sm.units[us] = info;
+        mbar_arrive(bar_at(sm, B_UNIT_FULL + us));
+      }
+      __syncwarp();
+    }
+    if (!acquire(bar_at(sm, B_UNIT_FULL + us), uph, E_LOAD_UNIT_FULL)) break;
+    const int4 info = sm.units[us];
+    if (info.y < 0) break;
+    const int off = info.x, n = info.y, q0 = info.z, head = info.w;
+    const int nkv = (n + kTile - 1) / kTile;
+    // K0/V0 first: they may land while the previous unit's last MMAs still
+    // hold the Q buffers.
+    if (!load_kv(0, n, off, head)) break;
+    if (!acquire(bar_at(sm, B_Q_EMPTY), (unit_iter & 1) ^ 1, E_LOAD_Q_EMPTY)) break;
+    load_tile(prm.q, sm.q0, q0, n, off, head);
+    if (q0 + kTile < n) load_tile(prm.q, sm.q0 + kTileBytes, q0 + kTile, n, off, head);
+    rotate(bar_at(sm, B_Q_FULL));
+    bool ok = true;
+    for (int j = 1; j < nkv && ok; ++j) ok = load_kv(j, n, off, head);
+    if (!ok) break;
+    flush();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_at(sm, B_UNIT_EMPTY + us));
+    ++unit_iter;
+  }
+  flush();
+}
+
+// One thread issues every MMA.  Per key tile j:
+//   S0 = Q0 K_j^T ; [PV1 of tile j-1] ; S1 = Q1 K_j^T ; PV0 of tile j
+// so the softmax of one Q tile overlaps the MMAs of the other.  S_t of tile
+// j+1 overwrites P_t of tile j only after PV_t(j) was issued (tcgen05.mma
+// from one thread execute in order).
+__device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, uint32_t tmem) {
+  int* err = prm.work + WS_ERROR;
+  const uint32_t tS0 = tmem + kColS0, tS1 = tmem + kColS1, tO0 = tmem + kColO0, tO1 = tmem + kColO1;
+  const uint32_t sQ1 = sm.q0 + kTileBytes;
+  uint32_t ring_iter = 0, unit_iter = 0, p_cnt0 = 0, p_cnt1 = 0;
+  while (true) {
+    const int us = unit_iter & 1;
+    if (!wait_bar(bar_at(sm, B_UNIT_FULL + us), (unit_iter >> 1) & 1, err, E_MMA_UNIT_FULL)) break;
+    const int4 info = sm.units[us];
+    if (info.y < 0) break;
+    const int n = info.y, q0 = info.z;
+    const bool has1 = q0 + kTile < n;
+    const int nkv = (n + kTile - 1) / kTile;
+    bool ok = true;
+    uint32_t v_prev = 0, vslot_prev = 0;
+    for (int j = 0; j < nkv; ++j) {
+      const uint32_t kslot = ring_iter % kSlots;
+      if (!(ok = wait_bar(bar_at(sm, B_RING_FULL + kslot), (ring_iter / kSlots) & 1, err, E_MMA_K_FULL))) break;
+      if (j == 0 && !(ok = wait_bar(bar_at(sm, B_Q_FULL), unit_iter & 1, err, E_MMA_Q_FULL))) break;
+      tc_fence_after();
+      const uint32_t kt = sm.ring + kslot * kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, desc_kmajor(sm.q0, kk), desc_kmajor(kt, kk), kIdescS, kk > 0);
+      tc_commit(bar_at(sm, B_S_FULL + 0));
+      if (j > 0) {
+        if (has1) {
+          if (!(ok = wait_bar(bar_at(sm, B_P_FULL + 1), p_cnt1 & 1, err, E_MMA_P1))) break;
+          ++p_cnt1;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tO1, tS1 + 8 * kk, desc_v(v_prev, kk), kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar_at(sm, B_RING_EMPTY + vslot_prev));
+      }
+      if (has1) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, desc_kmajor(sQ1, kk), desc_kmajor(kt, kk), kIdescS, kk > 0);
+        tc_commit(bar_at(sm, B_S_FULL + 1));
+      }
+      tc_commit(bar_at(sm, B_RING_EMPTY + kslot));
+      if (j == nkv - 1) tc_commit(bar_at(sm, B_Q_EMPTY));
+      ++ring_iter;
+      const uint32_t vslot = ring_iter % kSlots;
+      if (!(ok = wait_bar(bar_at(sm, B_RING_FULL + vslot), (ring_iter / kSlots) & 1, err, E_MMA_V_FULL))) break;
+      if (!(ok = wait_bar(bar_at(sm, B_P_FULL + 0), p_cnt0 & 1, err, E_MMA_P0))) break;
+      ++p_cnt0;
+      tc_fence_after();
+      const uint32_t vt = sm.ring + vslot * kTileBytes;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) mma_ts(tO0, tS0 + 8 * kk, desc_v(vt, kk), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      ++ring_iter;
+      v_prev = vt;
+      vslot_prev = vslot;
+    }
+    if (!ok) break;
+    if (has1) {
+      if (!wait_bar(bar_at(sm, B_P_FULL + 1), p_cnt1 & 1, err, E_MMA_P1)) break;
+      ++p_cnt1;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tO1, tS1 + 8 * kk, desc_v(v_prev, kk), kIdescPV, (nkv > 1 || kk > 0) ? 1u : 0u);
+    }
+    tc_commit(bar_at(sm, B_RING_EMPTY + vslot_prev));
+    tc_commit(bar_at(sm, B_O_FULL + 0));
+    if (has1) tc_commit(bar_at(sm, B_O_FULL + 1));
+    mbar_arrive(bar_at(sm, B_UNIT_EMPTY + us));
+    ++unit_iter;
+  }
+  // Drain: every MMA issued so far must finish before TMEM is freed.
+  tc_commit(bar_at(sm, B_DRAIN));
+  wait_bar(bar_at(sm, B_DRAIN), 0, err, E_MMA_DRAIN);
+}
+
+// Softmax warps: warp w handles Q tile w/4, TMEM lanes 32*(w%4) .. +31; the
+// thread owns one query row.
+__device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm, uint32_t tmem, int warp,
+                                             int lane) {
+  int* err = prm.work + WS_ERROR;
+  const int t = warp >> 2;
+  const int rq = (warp & 3) * 32 + lane;
+  const uint32_t lane_bits = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_bits + (t ? kColS1 : kColS0);
+  const uint32_t tO = tmem + lane_bits + (t ? kColO1 : kColO0);
+  const float c = prm.c;
+  uint32_t unit_iter = 0, s_iter = 0, o_iter = 0;
+  while (true) {
+    const int us = unit_iter & 1;
+    if (!__all_sync(0xffffffffu, wait_bar(bar_at(sm, B_UNIT_FULL + us), (unit_iter >> 1) & 1, err, E_SM_UNIT_FULL)))
+      break;
+    const int4 info = sm.units[us];
+    if (info.y < 0) break;
+    const int off = info.x, n = info.y, q0 = info.z, head = info.w;
+    if (t == 0 || q0 + kTile < n) {
+      const int nkv = (n + kTile - 1) / kTile;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar_at(sm, B_S_FULL + t), s_iter & 1, err, E_SM_S_FULL));
+        ++s_iter;
+        if (!ok) break;
+        tc_fence_after();
+        const int kv_valid = min(kTile, n - j * kTile);
+        float x[64];
+        float mx = -INFINITY;
+        tmem_ld64(tS, x);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i < kv_valid) mx = fmaxf(mx, x[i]);
+        tmem_ld64(tS + 64, x);
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (64 + i < kv_valid) mx = fmaxf(mx, x[i]);
+        const float m_new = fmaxf(m, mx * c);
+        if (j == 0) {
+          m = m_new;
+        } else if (__any_sync(0xffffffffu, m_new > m + kRescaleLog2)) {
+          const float alpha = ex2(m - m_new);
+          l *= alpha;
+          m = m_new;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tmem_ld64(tO + 64 * h, x);
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(x[i] * alpha);
+            tmem_st32(tO + 64 * h, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(x[32 + i] * alpha);
+            tmem_st32(tO + 64 * h + 32, r);
+          }
+          tmem_wait_st();
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld64(tS + 64 * h, x);
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = 64 * h + 2 * i;
+            const float p0 = col < kv_valid ? ex2(fmaf(x[2 * i], c, -m)) : 0.f;
+            const float p1 = col + 1 < kv_valid ? ex2(fmaf(x[2 * i + 1], c, -m)) : 0.f;
+            l += p0 + p1;
+            pk[i] = pack_bf16(p0, p1);
+          }
+          // P (bf16 pairs) over the S columns already read: tile half h of S
+          // (columns 64h..64h+63) becomes P columns 32h..32h+31.
+          tmem_st32(tS + 32 * h, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_at(sm, B_P_FULL + t));
+      }
+      if (!ok) break;
+      if (!__all_sync(0xffffffffu, wait_bar(bar_at(sm, B_O_FULL + t), o_iter & 1, err, E_SM_O_FULL))) break;
+      ++o_iter;
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const int qr = q0 + kTile * t + rq;
+      const bool valid = qr < n;
+      long long tok = 0;
+      if (valid) tok = prm.row_map ? __ldg(prm.row_map + off + qr) : off + qr;
+      uint4* dst = reinterpret_cast<uint4*>(prm.o + tok * prm.row_stride + static_cast<long long>(head) * (kD * 2));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x[64];
+        __syncwarp();
+        tmem_ld64(tO + 64 * h, x);
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(x[2 * i] * inv, x[2 * i + 1] * inv);
+        if (valid) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) dst[8 * h + k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+      tc_fence_before();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_at(sm, B_UNIT_EMPTY + us));
+    ++unit_iter;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const TcParams prm) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  Smem sm;
+  sm.q0 = base + kSmemQ;
+  sm.ring = base + kSmemRing;
+  sm.bars = base + kSmemBars;
+  sm.units = reinterpret_cast<int4*>(base_ptr + kSmemUnits);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + kSmemTmem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar_at(sm, B_RING_FULL + s), 4);
+      mbar_init(bar_at(sm, B_RING_EMPTY + s), 1);
+    }
+    mbar_init(bar_at(sm, B_Q_FULL), 4);
+    mbar_init(bar_at(sm, B_Q_EMPTY), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_at(sm, B_S_FULL + t), 1);
+      mbar_init(bar_at(sm, B_P_FULL + t), 128);
+      mbar_init(bar_at(sm, B_O_FULL + t), 1);
+      mbar_init(bar_at(sm, B_UNIT_FULL + t), 1);
+      mbar_init(bar_at(sm, B_UNIT_EMPTY + t), 4 + 1 + 8);
+    }
+    mbar_init(bar_at(sm, B_DRAIN), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp < kLoaderWarp0) {
+    softmax_role(prm, sm, tmem, warp, lane);
+  } else if (warp < kMmaWarp) {
+    loader_role(prm, sm, warp - kLoaderWarp0, lane);
+    cp_async_wait_all();
+  } else if (lane == 0) {
+    mma_role(prm, sm, tmem);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    // The last CTA to finish resets the scheduler for the next launch.
+    __threadfence();
+    const int prev = atomicAdd(prm.work + WS_DONE_CTAS, 1);
+    if (prev == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(prm.work + WS_NEXT_UNIT, 0);
+      atomicExch(prm.work + WS_DONE_CTAS, 0);
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attention_bf16_tc(const wsa_plan_s& p, const void* q, const void* k, const void* v, void* o,
+                                     int heads, bool canonical, float scale, cudaStream_t s) {
+  TcParams prm;
+  prm.q = static_cast<const char*>(q);
+  prm.k = static_cast<const char*>(k);
+  prm.v = static_cast<const char*>(v);
+  prm.o = static_cast<char*>(o);
+  prm.row_map = canonical ? p.d_ids : nullptr;
+  prm.offsets = p.d_offsets;
+  prm.items = p.d_tc_items;
+  prm.num_units = p.num_tc_items * heads;
+  prm.heads = heads;
+  prm.row_stride = static_cast<long long>(heads) * kD * 2;
+  prm.c = scale * 1.4426950408889634f;
+  prm.work = p.d_work;
+  cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(sm_count(), prm.num_units));
+  attention_tc_kernel<<<grid, kThreads, kSmemAlloc, s>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace wsa

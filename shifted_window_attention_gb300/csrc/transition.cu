@@ -1,0 +1,78 @@
+// Layout transition: the local permutation between two window layouts.
+//
+// "Window-Aligned Sequence Parallelism (SeedVR2)", sections "Motivation" and
+// "Plan A redistribution": with one rank, moving the activations from one
+// layout to the next is a permutation of rows.  Destination row p holds the
+// token at packed position p of the destination plan, which the source plan
+// stores at row pos_src[ids_dst[p]].
+//
+// The kernel is pure data movement and HBM-bound: every byte is read once and
+// written once.  One warp moves one row at a time with 16-byte vector loads,
+// keeping up to kVecPerLane loads in flight per lane before it stores them;
+// the two table lookups per row hit L2.  Loads and stores use the streaming
+// cache hints since neither side is reused.
+
+#include <algorithm>
+
+#include "wsa_internal.h"
+
+namespace wsa {
+namespace {
+
+constexpr int kVecPerLane = 12;      // 12 x 16 B x 32 lanes = one 6 KB row per pass
+constexpr int kThreads = 256;
+
+template <typename Vec>
+__global__ void __launch_bounds__(kThreads)
+transition_rows_kernel(const Vec* __restrict__ src, Vec* __restrict__ dst,
+                       const int* __restrict__ ids_dst, const int* __restrict__ pos_src,
+                       int n_rows, int vec_per_row) {
+  const int lane = threadIdx.x & 31;
+  const int warps_per_block = kThreads / 32;
+  const long long warp0 = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
+  const long long nwarps = static_cast<long long>(gridDim.x) * warps_per_block;
+  for (long long row = warp0; row < n_rows; row += nwarps) {
+    const int g = __ldg(pos_src + __ldg(ids_dst + row));
+    const Vec* s = src + static_cast<long long>(g) * vec_per_row;
+    Vec* d = dst + row * vec_per_row;
+    for (int base = 0; base < vec_per_row; base += 32 * kVecPerLane) {
+      Vec buf[kVecPerLane];
+#pragma unroll
+      for (int i = 0; i < kVecPerLane; ++i) {
+        const int c = base + i * 32 + lane;
+        if (c < vec_per_row) buf[i] = __ldcs(s + c);
+      }
+#pragma unroll
+      for (int i = 0; i < kVecPerLane; ++i) {
+        const int c = base + i * 32 + lane;
+        if (c < vec_per_row) __stcs(d + c, buf[i]);
+      }
+    }
+  }
+}
+
+template <typename Vec>
+cudaError_t launch_rows(const wsa_plan_s& src, const wsa_plan_s& dst, const void* x_src, void* x_dst,
+                        size_t row_bytes, cudaStream_t s) {
+  const int vec_per_row = static_cast<int>(row_bytes / sizeof(Vec));
+  const int sms = std::max(1, sm_count());
+  // 8 resident blocks of 256 threads per SM: 64 warps, the SM's limit.
+  const long long want = (static_cast<long long>(dst.num_tokens) + 7) / 8;
+  const int blocks = static_cast<int>(std::max(1LL, std::min<long long>(want, 8LL * sms)));
+  transition_rows_kernel<Vec><<<blocks, kThreads, 0, s>>>(
+      static_cast<const Vec*>(x_src), static_cast<Vec*>(x_dst), dst.d_ids, src.d_pos,
+      dst.num_tokens, vec_per_row);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_transition(const wsa_plan_s& src, const wsa_plan_s& dst, const void* x_src,
+                              void* x_dst, size_t row_bytes, cudaStream_t s) {
+  const auto a = reinterpret_cast<uintptr_t>(x_src) | reinterpret_cast<uintptr_t>(x_dst);
+  if (row_bytes % 16 == 0 && a % 16 == 0) return launch_rows<uint4>(src, dst, x_src, x_dst, row_bytes, s);
+  if (row_bytes % 4 == 0 && a % 4 == 0) return launch_rows<unsigned int>(src, dst, x_src, x_dst, row_bytes, s);
+  return launch_rows<unsigned short>(src, dst, x_src, x_dst, row_bytes, s);
+}
+
+}  // namespace wsa

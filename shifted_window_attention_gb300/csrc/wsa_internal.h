@@ -1,0 +1,79 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "wsa.h"
+
+namespace wsa {
+
+// Records `msg` as this thread's last error and returns `st`.
+wsa_status fail(wsa_status st, const std::string& msg);
+// Maps a CUDA error to WSA_ERR_CUDA (or WSA_ERR_OOM) with context.
+wsa_status cuda_fail(cudaError_t e, const char* what);
+void clear_error();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// One unit of attention work: query rows [q_start, q_start + span) of a window.
+struct WorkItem {
+  int window;
+  int q_start;
+};
+
+// Words of the per-plan device workspace (int32 each).
+enum WorkspaceWord {
+  WS_NEXT_UNIT = 0,   // dynamic scheduler: next unit to hand out
+  WS_DONE_CTAS = 1,   // CTAs that finished (the last one resets both counters)
+  WS_ERROR = 2,       // first error code recorded by a kernel (0 = none)
+  WS_WORDS = 8
+};
+
+// Query rows covered by one work item of each attention kernel.
+constexpr int kTcItemRows = 256;    // tensor-core kernel: two 128-row tiles
+constexpr int kSimtItemRows = 64;   // fp32 CUDA-core kernel
+
+}  // namespace wsa
+
+struct wsa_plan_s {
+  int T = 0, H = 0, W = 0;
+  int wt = 0, wh = 0, ww = 0;
+  int layout = 0;
+  int num_windows = 0;
+  int num_tokens = 0;
+  int max_window_tokens = 0;
+  int device = 0;
+  std::vector<int> h_offsets;  // [num_windows + 1]
+  std::vector<int> h_dims;     // [num_windows * 6]
+  int num_tc_items = 0;
+  int num_simt_items = 0;
+  // device memory: one allocation carved into the tables below
+  void* d_block = nullptr;
+  int* d_offsets = nullptr;
+  int* d_dims = nullptr;
+  int* d_ids = nullptr;
+  int* d_pos = nullptr;
+  wsa::WorkItem* d_tc_items = nullptr;
+  wsa::WorkItem* d_simt_items = nullptr;
+  int* d_work = nullptr;       // WS_WORDS int32, zero-initialised
+};
+
+namespace wsa {
+
+// Launchers (asynchronous; arguments already validated by the ABI layer).
+cudaError_t launch_plan_tables(const wsa_plan_s& p, cudaStream_t s);
+cudaError_t launch_transition(const wsa_plan_s& src, const wsa_plan_s& dst, const void* x_src,
+                              void* x_dst, size_t row_bytes, cudaStream_t s);
+cudaError_t launch_attention_fp32(const wsa_plan_s& p, const float* q, const float* k,
+                                  const float* v, float* o, int heads, int head_dim,
+                                  bool canonical, float scale, cudaStream_t s);
+cudaError_t launch_attention_bf16_tc(const wsa_plan_s& p, const void* q, const void* k,
+                                     const void* v, void* o, int heads, bool canonical,
+                                     float scale, cudaStream_t s);
+
+}  // namespace wsa

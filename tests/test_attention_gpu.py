@@ -1,0 +1,188 @@
+"""GPU window attention against the fp64 oracle ("Window-Aligned Sequence
+Parallelism (SeedVR2)", section "Motivation": attention only inside a window).
+
+Tolerances: bf16 max-abs 2e-2 and relative RMS 1e-2; fp32 max-abs 1e-4."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import wsa_inputs
+from tests.helpers import assert_bf16_close, assert_fp32_close, to64
+from wsa_inputs import WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+MID = wsa_inputs.custom(8, 24, 40, 2, 2, 2, heads=2, head_dim=128, name="mid")          # windows up to 3588 tokens
+SMALL_BF16 = wsa_inputs.custom(4, 9, 16, 2, 9, 16, heads=3, head_dim=128, name="tiny-bf16")  # 4..50-token windows
+ONE_TOKEN = wsa_inputs.custom(2, 3, 4, 2, 52, 69, heads=2, head_dim=128, name="one-token")
+
+
+@pytest.fixture(scope="module")
+def wsa():
+    import shifted_window_attention_gb300 as m
+    return m
+
+
+def _grid(w):
+    return (w.T, w.H, w.W, w.nt, w.nh, w.nw)
+
+
+def _run(wsa, w, layout, dtype=None, layer=0, canonical=True):
+    p = wsa.Plan(*_grid(w), layout)
+    q, k, v = wsa_inputs.qkv(w, layer=layer)
+    if dtype is not None:
+        q, k, v = (t.to(dtype) for t in (q, k, v))
+    qg, kg, vg = (t.cuda() for t in (q, k, v))
+    o = wsa.attention(p, qg, kg, vg, canonical=canonical)
+    return p, (q, k, v), o
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_fp32_tiny_full(wsa, layout):
+    w = WORKLOADS["tiny"]
+    p, (q, k, v), o = _run(wsa, w, layout)
+    ref = oracle.window_attention(to64(q), to64(k), to64(v), oracle.make_plan(*_grid(w), layout))
+    assert_fp32_close(to64(o), ref, f"fp32 tiny layout {layout}")
+    assert p.device_status() == 0
+
+
+def test_fp32_head_dim_128(wsa):
+    w = wsa_inputs.custom(5, 10, 12, 2, 4, 4, heads=2, head_dim=128, dtype="fp32", name="fp32-128")
+    p, (q, k, v), o = _run(wsa, w, 1)
+    ref = oracle.window_attention(to64(q), to64(k), to64(v), oracle.make_plan(*_grid(w), 1))
+    assert_fp32_close(to64(o), ref, "fp32 d128")
+
+
+@pytest.mark.parametrize("w", [SMALL_BF16, MID], ids=lambda w: w.name)
+@pytest.mark.parametrize("layout", [0, 1])
+def test_bf16_full_compare(wsa, w, layout):
+    p, (q, k, v), o = _run(wsa, w, layout)
+    ref = oracle.window_attention(to64(q), to64(k), to64(v), oracle.make_plan(*_grid(w), layout))
+    assert_bf16_close(to64(o), ref, f"{w.name} layout {layout}")
+    assert p.device_status() == 0
+
+
+def test_packed_order_matches_canonical(wsa):
+    w = MID
+    p, (q, k, v), o = _run(wsa, w, 1)
+    ids = torch.from_numpy(oracle.make_plan(*_grid(w), 1).ids.astype(np.int64))
+    qp, kp, vp = (t[ids].contiguous().cuda() for t in (q, k, v))
+    op = wsa.attention(p, qp, kp, vp, canonical=False)
+    assert torch.equal(op.cpu(), o.cpu()[ids])
+
+
+def test_repeat_calls_identical(wsa):
+    w = MID
+    p, (q, k, v), o = _run(wsa, w, 0)
+    qg, kg, vg = (t.cuda() for t in (q, k, v))
+    for _ in range(3):
+        o2 = wsa.attention(p, qg, kg, vg)
+        assert torch.equal(o2, o)
+    assert p.device_status() == 0
+
+
+def test_isolation(wsa):
+    # Perturb one window's inputs: every other window's output stays bit-identical.
+    w = MID
+    p, (q, k, v), o = _run(wsa, w, 1)
+    op = oracle.make_plan(*_grid(w), 1)
+    win = op.num_windows // 2
+    rows = torch.from_numpy(op.ids[op.offsets[win]:op.offsets[win + 1]].astype(np.int64))
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    q2[rows] = -q2[rows]
+    k2[rows] = k2[rows] * 2
+    v2[rows] = v2[rows] + 1
+    o2 = wsa.attention(p, q2.cuda(), k2.cuda(), v2.cuda()).cpu()
+    mask = torch.ones(w.num_tokens, dtype=torch.bool)
+    mask[rows] = False
+    assert torch.equal(o2[mask], o.cpu()[mask])
+    assert not torch.equal(o2[rows], o.cpu()[rows])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_one_token_windows_give_v(wsa, dtype):
+    w = ONE_TOKEN
+    p, (q, k, v), o = _run(wsa, w, 0, dtype=dtype)
+    assert p.num_windows == w.num_tokens
+    assert torch.equal(o.cpu(), v)
+
+
+def test_constant_keys_mean_of_values(wsa):
+    w = MID
+    p = wsa.Plan(*_grid(w), 1)
+    q, k, v = wsa_inputs.qkv(w)
+    k = torch.full_like(k, 0.25)
+    o = wsa.attention(p, q.cuda(), k.cuda(), v.cuda())
+    ref = oracle.window_attention(to64(q), to64(k), to64(v), oracle.make_plan(*_grid(w), 1))
+    assert_bf16_close(to64(o), ref, "constant keys")
+
+
+def _sample_windows(op, count, seed):
+    n = np.diff(op.offsets)
+    rng = np.random.default_rng(seed)
+    picks = {int(np.argmin(n)), int(np.argmax(n)), 0, op.num_windows - 1}
+    picks |= set(int(x) for x in rng.choice(op.num_windows, size=min(count, op.num_windows), replace=False))
+    return sorted(picks)
+
+
+def _check_sampled(wsa, w, layout, layer=0, windows=6, heads_per_window=3, seed=0):
+    g = _grid(w)
+    p = wsa.Plan(*g, layout)
+    op = oracle.make_plan(*g, layout)
+    q, k, v = wsa_inputs.qkv(w, layer=layer, device="cuda")
+    o = torch.full_like(q, float("nan"))
+    wsa.attention(p, q, k, v, out=o)
+    assert p.device_status() == 0
+    # every output row of every head was written and is finite
+    assert bool(torch.isfinite(o).all())
+    qn, kn, vn, on = (t.float().cpu().numpy() for t in (q, k, v, o))
+    rng = np.random.default_rng(seed + layer)
+    worst = (0.0, 0.0)
+    for win in _sample_windows(op, windows, seed + layer):
+        n = int(op.offsets[win + 1] - op.offsets[win])
+        rows = op.ids[op.offsets[win]:op.offsets[win + 1]].astype(np.int64)
+        for h in rng.choice(w.heads, size=heads_per_window, replace=False):
+            ref = oracle.window_attention_rows(qn, kn, vn, op, win, int(h), np.arange(n))
+            e = assert_bf16_close(on[rows, int(h), :], ref, f"{w.name} L{layout} win {win} head {h}")
+            worst = (max(worst[0], e[0]), max(worst[1], e[1]))
+    return worst
+
+
+@pytest.mark.parametrize("name", ["720p", "1080p", "long"])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_full_size_sampled(wsa, name, layout):
+    _check_sampled(wsa, WORKLOADS[name], layout)
+
+
+def test_32layer_schedule_sampled(wsa):
+    # alternating layouts, fresh Q/K/V per layer; layers 0 and 1 plus a seeded
+    # sample of later layers
+    w = WORKLOADS["32layer"]
+    for layer in (0, 1, 2, 13, 30, 31):
+        _check_sampled(wsa, w, layer % 2, layer=layer, windows=3, heads_per_window=2)
+
+
+def test_argument_errors(wsa):
+    w = SMALL_BF16
+    p = wsa.Plan(*_grid(w), 0)
+    q = torch.zeros(w.num_tokens, 2, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(wsa.WsaError) as e:
+        wsa.attention(p, q, q.clone(), q.clone())
+    assert e.value.name == "WSA_ERR_UNSUPPORTED"
+    q = torch.zeros(w.num_tokens * 2 * 128 + 8, device="cuda", dtype=torch.bfloat16)
+    qv = q[1:1 + w.num_tokens * 2 * 128]
+    st = wsa.lib.wsa_attention(p.handle, ctypes.c_void_p(qv.data_ptr()), ctypes.c_void_p(qv.data_ptr()),
+                               ctypes.c_void_p(qv.data_ptr()), ctypes.c_void_p(q.data_ptr() + 64), 2, 128, 0, 1,
+                               0.0, None)
+    assert st == -1  # misaligned
+    x = torch.zeros(w.num_tokens, 2, 128, device="cuda", dtype=torch.bfloat16)
+    st = wsa.lib.wsa_attention(p.handle, ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(x.data_ptr()),
+                               ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(x.data_ptr()), 2, 128, 0, 1, 0.0, None)
+    assert st == -1  # output aliases input
+    with pytest.raises(wsa.WsaError):
+        wsa.attention(p, x[:-1].contiguous(), x[:-1].contiguous(), x[:-1].contiguous())
+    assert p.device_status() == 0
