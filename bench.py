@@ -114,6 +114,10 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = wsa_inputs.WORKLOADS[args.workload]
+    if args.heads:
+        # same grid, fewer heads: the small case used for detailed profiles
+        wl = wsa_inputs.Workload(f"{wl.name}-{args.heads}h", wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw,
+                                 args.heads, wl.head_dim, wl.dtype, wl.dist)
     g = (wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw)
     N, C = wl.num_tokens, wl.channels
 
@@ -184,6 +188,9 @@ def run_ours(args):
     # End to end through the public API with pinned host buffers: H2D of this
     # step's Q/K/V (both layers) and hidden rows, the three calls, D2H of the
     # two attention outputs and the transitioned rows.
+    if args.no_e2e:
+        return finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, ms_step, None,
+                      trans_bytes, clk, plan_ms, N, dist)
     host_in = [t.cpu().pin_memory() for t in (q0, k0, v0, q1, k1, v1, x)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o0, o1, y)]
     dev_in = [q0, k0, v0, q1, k1, v1, x]
@@ -218,6 +225,14 @@ def run_ours(args):
     if reg.device_status() or sft.device_status():
         raise RuntimeError("device error during the timed region")
 
+    e2e = {"value": round(ws * (fl_r + fl_s) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    return finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, ms_step, e2e,
+                  trans_bytes, clk, plan_ms, N, dist)
+
+
+def finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, ms_step, e2e,
+           trans_bytes, clk, plan_ms, N, dist):
     peaks, peak_kind = load_peaks()
     attn_ms = (np.mean(a_r) + np.mean(a_s)) / 2
     fl_launch = (fl_r + fl_s) / 2
@@ -263,8 +278,7 @@ def run_ours(args):
             "peak_source": f"{peak_kind} bf16 burst",
             "traffic": None,
         },
-        "e2e": {"value": round(ws * (fl_r + fl_s) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
     }
@@ -352,6 +366,8 @@ def main():
     ap.add_argument("--workload", default="720p")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--heads", type=int, default=0, help="override the head count (small profiling case)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -98,12 +98,13 @@ def layout_windows(T, H, W, nt, nh, nw, layout, max_temporal=30):
 
 
 class _DeviceArray:
-    """Zero-copy view of a library-owned int32 device table."""
+    """Zero-copy view of a library-owned int32 device table (read-only by the
+    library's contract; torch does not model the read-only flag)."""
 
     def __init__(self, ptr, n, owner):
         self._owner = owner  # keeps the plan alive while the view exists
         self.__cuda_array_interface__ = {
-            "shape": (n,), "typestr": "<i4", "data": (ptr, True), "version": 3, "strides": None,
+            "shape": (n,), "typestr": "<i4", "data": (ptr, False), "version": 3, "strides": None,
         }
 
 

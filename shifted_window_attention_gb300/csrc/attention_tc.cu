@@ -25,7 +25,8 @@
 //  * Online softmax in the log2 domain with a lazy rescale: the running max is
 //    only raised (and O rescaled in TMEM) when a row's max grows by more than
 //    2^8, which keeps every probability <= 256 and the result exact up to
-//    rounding.
+//    rounding.  The row sum accumulates the same bf16-rounded probabilities
+//    that enter the P V product.
 //  * Every wait is bounded: after ~1 s a wait records an error code in the
 //    plan's workspace and the CTA unwinds, drains its MMAs and cp.asyncs and
 //    frees TMEM.
@@ -531,8 +532,11 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
             const int col = 64 * h + 2 * i;
             const float p0 = col < kv_valid ? ex2(fmaf(x[2 * i], c, -m)) : 0.f;
             const float p1 = col + 1 < kv_valid ? ex2(fmaf(x[2 * i + 1], c, -m)) : 0.f;
-            l += p0 + p1;
             pk[i] = pack_bf16(p0, p1);
+            // The row sum uses the bf16-rounded P that the P V product sees, so
+            // the output is an exact convex combination of V rows up to fp32
+            // accumulation (matters for peaked rows where |O| approaches |V|).
+            l += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
           }
           // P (bf16 pairs) over the S columns already read: tile half h of S
           // (columns 64h..64h+63) becomes P columns 32h..32h+31.
