@@ -143,6 +143,42 @@ wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src,
                           void* x_dst, int channels, wsa_dtype dtype, void* stream);
 
 /*
+ * wsa_attention_noalloc -- the bf16 window attention of wsa_attention for
+ * callers that cannot allocate device memory.  The pages have no counterpart:
+ * this is a deployment convenience of this library.
+ *
+ * Some callers cannot call cudaMalloc: their device memory is owned by
+ * another framework's pool, their serving loop must not take the device-wide
+ * synchronisation that cudaMalloc/cudaFree imply, or they run while a stream
+ * is being captured.  They cannot create a plan, so this call takes the grid
+ * (T, H, W, nt, nh, nw, layout, max_temporal as in wsa_plan_create) directly
+ * and builds the plan tables itself in a fixed device array inside the
+ * library, then runs the same tensor-core attention kernel.  It allocates no
+ * device memory: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * q, k, v, o, heads, in_order_canonical, softmax_scale and stream as in
+ * wsa_attention with dtype WSA_BF16 and head_dim 128 (fixed).
+ *
+ * Limits of the fixed array (about 4.4 MB, held by every GPU that loads the
+ * library until the process exits): T*H*W <= 524288 tokens, at most 8192
+ * windows and 16384 work items of 256 query rows; beyond them the call
+ * returns WSA_ERR_UNSUPPORTED with a message naming the limit.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call reuses the same array and overwrites what the previous
+ * call left there, so calls whose GPU work overlaps (other streams, other
+ * host threads) race and must be ordered by the caller.  A device-side wait
+ * that gives up is not reported by this call (use wsa_attention with a plan
+ * and wsa_plan_device_status for that).
+ */
+wsa_status wsa_attention_noalloc(int T, int H, int W, int nt, int nh, int nw,
+                                 wsa_layout layout, int max_temporal,
+                                 const void* q, const void* k, const void* v,
+                                 void* o, int heads, int in_order_canonical,
+                                 float softmax_scale, void* stream);
+
+/*
  * Reads and clears the plan's device error word (synchronises the device).
  * *code = 0 when no kernel recorded an error; otherwise the code of the first
  * bounded wait that gave up, and the call returns WSA_ERR_DEVICE_CHECK.

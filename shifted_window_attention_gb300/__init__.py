@@ -56,6 +56,7 @@ def _load():
         "wsa_attention": ([p, p, p, p, p, i, i, i, i, f, p], i),
         "wsa_transition": ([p, p, p, p, i, i, p], i),
         "wsa_plan_device_status": ([p, ip], i),
+        "wsa_attention_noalloc": ([i] * 8 + [p, p, p, p, i, i, f, p], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -208,7 +209,23 @@ def transition(src, dst, x, out=None, stream=None):
     return out
 
 
+def attention_noalloc(T, H, W, nt, nh, nw, layout, q, k, v, out, canonical=True, scale=0.0,
+                      max_temporal=30, stream=None):
+    """wsa_attention_noalloc: bf16 window attention of one layout without a
+    plan and without any device allocation (for callers that cannot allocate
+    device memory).  ``out`` must be provided by the caller."""
+    for t in (q, k, v, out):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 3 or t.dtype != torch.bfloat16:
+            raise WsaError(-1, "q, k, v, out must be contiguous 3-D bf16 CUDA tensors")
+    if k.shape != q.shape or v.shape != q.shape or out.shape != q.shape or q.shape[2] != 128:
+        raise WsaError(-1, "q, k, v, out must share the shape [N, heads, 128]")
+    _check(lib.wsa_attention_noalloc(T, H, W, nt, nh, nw, layout, max_temporal, _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(out), q.shape[1], 1 if canonical else 0, float(scale),
+                                     _stream(stream)))
+    return out
+
+
 __all__ = [
     "REGULAR", "SHIFTED", "BF16", "FP32", "WsaError", "Plan", "attention", "transition",
-    "window_size", "layout_windows", "version", "lib",
+    "window_size", "layout_windows", "version", "lib", "attention_noalloc",
 ]

@@ -55,6 +55,11 @@ namespace {
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+}  // namespace
+
+// Host geometry, shared with the other translation units through
+// wsa_internal.h.
+
 // Window size in fp64 exactly as the note's formula reads; nearbyint rounds
 // half-to-even in the default rounding mode (Python's round).
 wsa_status window_size(int T, int H, int W, int nt, int nh, int nw, int max_temporal,
@@ -135,6 +140,8 @@ std::vector<WorkItem> make_items(const std::vector<int>& offsets, int rows, int 
   for (const auto& k : v) out.push_back(k.it);
   return out;
 }
+
+namespace {
 
 // One thread per packed position: find the window by binary search on the
 // offsets, decode the row-major (dt, dh, dw) inside its box, write the

@@ -34,3 +34,16 @@ def assert_fp32_close(got, ref, what=""):
     max_abs, _ = errors(got, ref)
     assert max_abs <= FP32_MAX_ABS, f"{what}: max_abs={max_abs:.3e} (<= {FP32_MAX_ABS})"
     return max_abs
+
+
+def assert_bf16_close_torch(got, ref, what=""):
+    """The bf16 tolerance check evaluated on the GPU (large tensors)."""
+    import math
+    g = got.float()
+    r = ref.float()
+    d = g - r
+    max_abs = float(d.abs().max())
+    rel_rms = float(d.pow(2).mean().sqrt()) / max(float(r.pow(2).mean().sqrt()), 1e-30)
+    assert math.isfinite(max_abs) and max_abs <= BF16_MAX_ABS and rel_rms <= BF16_REL_RMS, (
+        f"{what}: max_abs={max_abs:.3e} (<= {BF16_MAX_ABS}), rel_rms={rel_rms:.3e} (<= {BF16_REL_RMS})")
+    return max_abs, rel_rms
