@@ -15,9 +15,9 @@
 //    by an atomic counter in heaviest-first order (the note's LPT rule applied
 //    to kernel work units), so ragged edge windows fill the tail.
 //  * Warp roles: warps 0-3 run the softmax of Q tile 0 and warps 4-7 that of
-//    Q tile 1 (one query row per thread = one TMEM lane); warps 8-11 gather
+//    Q tile 1 (one query row per thread = one TMEM lane); warps 8-9 gather
 //    Q/K/V rows with 16-byte cp.async into 128B-swizzled shared-memory tiles;
-//    one thread of warp 12 issues every tcgen05.mma.
+//    one thread of warp 10 issues every tcgen05.mma.
 //  * TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The bf16
 //    probabilities P overwrite the first 64 columns of their S tile and feed
 //    the P V product straight from TMEM (A operand in TMEM); V is the B
@@ -47,8 +47,10 @@ constexpr int kTileBytes = kTile * kD * 2;  // 32 KB
 constexpr int kPanelBytes = kTile * 128;    // 128 rows x 128 B (64 channels), one swizzle panel
 constexpr int kSlots = 4;                   // K/V ring slots
 constexpr int kLoaderWarp0 = 8;
-constexpr int kMmaWarp = 12;
-constexpr int kThreads = 13 * 32;
+constexpr int kLoaderWarps = 2;
+constexpr int kLoaderRows = kTile / kLoaderWarps;  // 64 rows of each tile per gather warp
+constexpr int kMmaWarp = kLoaderWarp0 + kLoaderWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;       // 11 warps: at most 3 per SM sub-partition
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 
@@ -139,7 +141,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 
 // Bounded wait on an mbarrier phase.  Gives up when another thread has
 // recorded an error, or after kWaitCycles, recording `code` first.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* err, int code) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* err, int code) {
   if (mbar_try(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
@@ -245,6 +247,35 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
   for (int i = 0; i < 64; ++i) x[i] = __uint_as_float(r[i]);
 }
 
+// 128 consecutive fp32 columns in one load (one wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&x)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : WSA_R8(0), WSA_R8(8), WSA_R8(16), WSA_R8(24), WSA_R8(32), WSA_R8(40), WSA_R8(48), WSA_R8(56),
+        WSA_R8(64), WSA_R8(72), WSA_R8(80), WSA_R8(88), WSA_R8(96), WSA_R8(104), WSA_R8(112), WSA_R8(120)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&x)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,"
+      "%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : WSA_R8(0), WSA_R8(8), WSA_R8(16), WSA_R8(24)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -276,8 +307,8 @@ struct Smem {
 
 __device__ __forceinline__ uint32_t bar_at(const Smem& s, int i) { return s.bars + 8u * static_cast<uint32_t>(i); }
 
-// Gather warps (4): rows 32*lw .. 32*lw+31 of every tile.  A half-warp copies
-// one 256-byte row (16 chunks of 16 bytes), so each lane issues 16 cp.async
+// Gather warps (2): rows 64*lw .. 64*lw+63 of every tile.  A half-warp copies
+// one 256-byte row (16 chunks of 16 bytes), so each lane issues 32 cp.async
 // per tile.  Shared layout: two 64-channel panels of 128 rows x 128 bytes,
 // chunk c of row r stored at chunk position c ^ (r % 8) (128-byte swizzle).
 __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm, int lw, int lane) {
@@ -318,14 +349,19 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     return __all_sync(0xffffffffu, wait_bar(bar, parity, err, code));
   };
   auto load_tile = [&](const char* src, uint32_t dst, int row0, int n, int off, int head) {
-    const int myrow = row0 + 32 * lw + lane;
-    int myid = -1;
-    if (myrow < n) myid = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+    // lane l looks up the ids of rows kLoaderRows*lw + l and + 32 + l
+    int myid[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int myrow = row0 + kLoaderRows * lw + 32 * h + lane;
+      myid[h] = -1;
+      if (myrow < n) myid[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+    }
     const char* colbase = src + static_cast<long long>(head) * (kD * 2) + chunk * 16;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int r = 32 * lw + half + 2 * i;
-      const int id = __shfl_sync(0xffffffffu, myid, half + 2 * i);
+    for (int i = 0; i < 32; ++i) {
+      const int r = kLoaderRows * lw + half + 2 * i;
+      const int id = __shfl_sync(0xffffffffu, myid[i >> 4], half + 2 * (i & 15));
       const char* g = id >= 0 ? colbase + static_cast<long long>(id) * prm.row_stride : src;
       cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
     }
@@ -464,6 +500,87 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
   wait_bar(bar_at(sm, B_DRAIN), 0, err, E_MMA_DRAIN);
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// One key tile of the online softmax for this thread's query row: reads the
+// 128 scores of S, updates the running max m (log2 domain, lazily) and the
+// running sum l2 (two partial sums), rescales O in TMEM when the max grows by
+// more than 2^8, and writes the bf16 probabilities P over the first 64
+// columns of S.  kFull: all 128 key columns are valid (no masking).
+template <bool kFull>
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool first, int kv_valid, float c,
+                                             float& m, float2& la, float2& lb) {
+  float x[128];
+  tmem_ld128(tS, x);
+  float mx;
+  if (kFull) {
+    float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
+#pragma unroll
+    for (int i = 4; i < 128; i += 8) {
+      m0 = fmax3(m0, x[i], x[i + 1]);
+      m1 = fmax3(m1, x[i + 2], x[i + 3]);
+      m2 = fmax3(m2, x[i + 4], x[i + 5]);
+      m3 = fmax3(m3, x[i + 6], x[i + 7]);
+    }
+    mx = fmax3(m0, m1, fmaxf(m2, m3));
+  } else {
+    mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 128; ++i)
+      if (i < kv_valid) mx = fmaxf(mx, x[i]);
+  }
+  const float m_new = fmaxf(m, mx * c);
+  if (first) {
+    m = m_new;
+  } else if (__any_sync(0xffffffffu, m_new > m + kRescaleLog2)) {
+    const float alpha = ex2(m - m_new);
+    la = __fmul2_rn(la, make_float2(alpha, alpha));
+    lb = __fmul2_rn(lb, make_float2(alpha, alpha));
+    m = m_new;
+#pragma unroll 1
+    for (int h = 0; h < 4; ++h) {
+      float o[32];
+      tmem_ld32(tO + 32 * h, o);
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(o[i] * alpha);
+      tmem_st32(tO + 32 * h, r);
+    }
+    tmem_wait_st();
+    // Rare path: the scores are read again instead of being kept live across
+    // the rescale, which keeps the register budget of the common path.
+    tmem_ld128(tS, x);
+  }
+  const float2 cc = make_float2(c, c);
+  const float2 nm = make_float2(-m, -m);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = 64 * h + 2 * i;
+      const float2 a = __ffma2_rn(make_float2(x[e], x[e + 1]), cc, nm);
+      float p0 = ex2(a.x), p1 = ex2(a.y);
+      if (!kFull) {
+        p0 = e < kv_valid ? p0 : 0.f;
+        p1 = e + 1 < kv_valid ? p1 : 0.f;
+      }
+      pk[i] = pack_bf16(p0, p1);
+      // The row sum uses the bf16-rounded P that the P V product sees, so the
+      // output is an exact convex combination of V rows up to fp32
+      // accumulation (matters for peaked rows where |O| approaches |V|).
+      const float2 r = make_float2(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u));
+      if (i & 1) lb = __fadd2_rn(lb, r); else la = __fadd2_rn(la, r);
+    }
+    // P (bf16 pairs): S columns 64h..64h+63 become P columns 32h..32h+31.
+    tmem_st32(tS + 32 * h, pk);
+  }
+}
+
 // Softmax warps: warp w handles Q tile w/4, TMEM lanes 32*(w%4) .. +31; the
 // thread owns one query row.
 __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm, uint32_t tmem, int warp,
@@ -485,7 +602,8 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
     const int off = info.x, n = info.y, q0 = info.z, head = info.w;
     if (t == 0 || q0 + kTile < n) {
       const int nkv = (n + kTile - 1) / kTile;
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY;
+      float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
       bool ok = true;
       for (int j = 0; j < nkv; ++j) {
         ok = __all_sync(0xffffffffu, wait_bar(bar_at(sm, B_S_FULL + t), s_iter & 1, err, E_SM_S_FULL));
@@ -493,55 +611,10 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
         if (!ok) break;
         tc_fence_after();
         const int kv_valid = min(kTile, n - j * kTile);
-        float x[64];
-        float mx = -INFINITY;
-        tmem_ld64(tS, x);
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i < kv_valid) mx = fmaxf(mx, x[i]);
-        tmem_ld64(tS + 64, x);
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (64 + i < kv_valid) mx = fmaxf(mx, x[i]);
-        const float m_new = fmaxf(m, mx * c);
-        if (j == 0) {
-          m = m_new;
-        } else if (__any_sync(0xffffffffu, m_new > m + kRescaleLog2)) {
-          const float alpha = ex2(m - m_new);
-          l *= alpha;
-          m = m_new;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tmem_ld64(tO + 64 * h, x);
-            uint32_t r[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(x[i] * alpha);
-            tmem_st32(tO + 64 * h, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(x[32 + i] * alpha);
-            tmem_st32(tO + 64 * h + 32, r);
-          }
-          tmem_wait_st();
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tmem_ld64(tS + 64 * h, x);
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = 64 * h + 2 * i;
-            const float p0 = col < kv_valid ? ex2(fmaf(x[2 * i], c, -m)) : 0.f;
-            const float p1 = col + 1 < kv_valid ? ex2(fmaf(x[2 * i + 1], c, -m)) : 0.f;
-            pk[i] = pack_bf16(p0, p1);
-            // The row sum uses the bf16-rounded P that the P V product sees, so
-            // the output is an exact convex combination of V rows up to fp32
-            // accumulation (matters for peaked rows where |O| approaches |V|).
-            l += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
-          }
-          // P (bf16 pairs) over the S columns already read: tile half h of S
-          // (columns 64h..64h+63) becomes P columns 32h..32h+31.
-          tmem_st32(tS + 32 * h, pk);
-        }
+        if (kv_valid == kTile)
+          softmax_tile<true>(tS, tO, j == 0, kv_valid, c, m, la, lb);
+        else
+          softmax_tile<false>(tS, tO, j == 0, kv_valid, c, m, la, lb);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_at(sm, B_P_FULL + t));
@@ -550,7 +623,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
       if (!__all_sync(0xffffffffu, wait_bar(bar_at(sm, B_O_FULL + t), o_iter & 1, err, E_SM_O_FULL))) break;
       ++o_iter;
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = 1.f / ((la.x + la.y) + (lb.x + lb.y));
       const int qr = q0 + kTile * t + rq;
       const bool valid = qr < n;
       long long tok = 0;
@@ -577,7 +650,9 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const TcParams prm) {
+// Registers: each SM sub-partition holds 16K registers and at most 3 of the
+// 11 warps, so 168 registers per thread fit (3 x 32 x 168 = 16,128).
+__global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -592,17 +667,17 @@ __global__ void __launch_bounds__(kThreads, 1) attention_tc_kernel(const TcParam
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(bar_at(sm, B_RING_FULL + s), 4);
+      mbar_init(bar_at(sm, B_RING_FULL + s), kLoaderWarps);
       mbar_init(bar_at(sm, B_RING_EMPTY + s), 1);
     }
-    mbar_init(bar_at(sm, B_Q_FULL), 4);
+    mbar_init(bar_at(sm, B_Q_FULL), kLoaderWarps);
     mbar_init(bar_at(sm, B_Q_EMPTY), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_at(sm, B_S_FULL + t), 1);
       mbar_init(bar_at(sm, B_P_FULL + t), 128);
       mbar_init(bar_at(sm, B_O_FULL + t), 1);
       mbar_init(bar_at(sm, B_UNIT_FULL + t), 1);
-      mbar_init(bar_at(sm, B_UNIT_EMPTY + t), 4 + 1 + 8);
+      mbar_init(bar_at(sm, B_UNIT_EMPTY + t), kLoaderWarps + 1 + 8);
     }
     mbar_init(bar_at(sm, B_DRAIN), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
