@@ -160,6 +160,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrives on `bar` once every cp.async issued so far by this thread has
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 // Makes this thread's completed generic-proxy shared-memory writes visible to
@@ -311,6 +316,11 @@ __device__ __forceinline__ uint32_t bar_at(const Smem& s, int i) { return s.bars
 // one 256-byte row (16 chunks of 16 bytes), so each lane issues 32 cp.async
 // per tile.  Shared layout: two 64-channel panels of 128 rows x 128 bytes,
 // chunk c of row r stored at chunk position c ^ (r % 8) (128-byte swizzle).
+// Completion is signalled asynchronously: after its copies for a tile, every
+// lane arms a cp.async arrive on the tile's full barrier (64 arrivals), so the
+// gather warps never wait for data; the MMA thread makes the landed rows
+// visible to the tensor core with a proxy fence.  The token ids of the next
+// key tile are fetched while the current one is issued.
 __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm, int lw, int lane) {
   int* err = prm.work + WS_ERROR;
   const int half = lane >> 4;
@@ -318,61 +328,37 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
   const uint32_t panel_off = static_cast<uint32_t>((chunk >> 3) * kPanelBytes);
   const int cc = chunk & 7;
   uint32_t ring_iter = 0, unit_iter = 0;
-  uint32_t pending = 0;
-  bool has_pending = false;  // warp-uniform
 
-  auto flush = [&]() {
-    if (has_pending) {
-      cp_async_wait_all();
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pending);
-      has_pending = false;
-    }
-  };
-  // Closes the copy group just issued; signals the previous group once it landed.
-  auto rotate = [&](uint32_t full_bar) {
-    cp_async_commit();
-    if (has_pending) {
-      cp_async_wait_1();
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pending);
-    }
-    pending = full_bar;
-    has_pending = true;
-  };
-  // Never blocks while a finished-but-unsignalled copy group is held back.
   auto acquire = [&](uint32_t bar, uint32_t parity, int code) -> bool {
-    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
-    flush();
     return __all_sync(0xffffffffu, wait_bar(bar, parity, err, code));
   };
-  auto load_tile = [&](const char* src, uint32_t dst, int row0, int n, int off, int head) {
-    // lane l looks up the ids of rows kLoaderRows*lw + l and + 32 + l
-    int myid[2];
+  // lane l holds the ids of rows kLoaderRows*lw + l and + 32 + l of a tile
+  // starting at window row row0 (-1: past the window end)
+  auto fetch_ids = [&](int (&ids)[2], int row0, int n, int off) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int myrow = row0 + kLoaderRows * lw + 32 * h + lane;
-      myid[h] = -1;
-      if (myrow < n) myid[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+      ids[h] = -1;
+      if (myrow < n) ids[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
     }
+  };
+  auto copy_tile = [&](const char* src, uint32_t dst, const int (&ids)[2], int head) {
     const char* colbase = src + static_cast<long long>(head) * (kD * 2) + chunk * 16;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int r = kLoaderRows * lw + half + 2 * i;
-      const int id = __shfl_sync(0xffffffffu, myid[i >> 4], half + 2 * (i & 15));
+      const int id = __shfl_sync(0xffffffffu, ids[i >> 4], half + 2 * (i & 15));
       const char* g = id >= 0 ? colbase + static_cast<long long>(id) * prm.row_stride : src;
       cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
     }
   };
-  auto load_kv = [&](int j, int n, int off, int head) -> bool {
+  auto load_kv = [&](const int (&ids)[2], int head) -> bool {
     for (int which = 0; which < 2; ++which) {
       const uint32_t slot = ring_iter % kSlots;
       if (!acquire(bar_at(sm, B_RING_EMPTY + slot), ((ring_iter / kSlots) & 1) ^ 1, E_LOAD_RING_EMPTY))
         return false;
-      load_tile(which ? prm.v : prm.k, sm.ring + slot * kTileBytes, j * kTile, n, off, head);
-      rotate(bar_at(sm, B_RING_FULL + slot));
+      copy_tile(which ? prm.v : prm.k, sm.ring + slot * kTileBytes, ids, head);
+      cp_async_arrive(bar_at(sm, B_RING_FULL + slot));
       ++ring_iter;
     }
     return true;
@@ -402,22 +388,32 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     if (info.y < 0) break;
     const int off = info.x, n = info.y, q0 = info.z, head = info.w;
     const int nkv = (n + kTile - 1) / kTile;
+    const bool has1 = q0 + kTile < n;
+    int ids[2], ids_next[2], qids0[2], qids1[2];
+    fetch_ids(ids, 0, n, off);
+    fetch_ids(qids0, q0, n, off);
+    if (has1) fetch_ids(qids1, q0 + kTile, n, off);
     // K0/V0 first: they may land while the previous unit's last MMAs still
     // hold the Q buffers.
-    if (!load_kv(0, n, off, head)) break;
+    if (nkv > 1) fetch_ids(ids_next, kTile, n, off);
+    if (!load_kv(ids, head)) break;
     if (!acquire(bar_at(sm, B_Q_EMPTY), (unit_iter & 1) ^ 1, E_LOAD_Q_EMPTY)) break;
-    load_tile(prm.q, sm.q0, q0, n, off, head);
-    if (q0 + kTile < n) load_tile(prm.q, sm.q0 + kTileBytes, q0 + kTile, n, off, head);
-    rotate(bar_at(sm, B_Q_FULL));
+    copy_tile(prm.q, sm.q0, qids0, head);
+    if (has1) copy_tile(prm.q, sm.q0 + kTileBytes, qids1, head);
+    cp_async_arrive(bar_at(sm, B_Q_FULL));
     bool ok = true;
-    for (int j = 1; j < nkv && ok; ++j) ok = load_kv(j, n, off, head);
+    for (int j = 1; j < nkv && ok; ++j) {
+      ids[0] = ids_next[0];
+      ids[1] = ids_next[1];
+      if (j + 1 < nkv) fetch_ids(ids_next, (j + 1) * kTile, n, off);
+      ok = load_kv(ids, head);
+    }
     if (!ok) break;
-    flush();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_at(sm, B_UNIT_EMPTY + us));
     ++unit_iter;
   }
-  flush();
+  cp_async_wait_all();
 }
 
 // One thread issues every MMA.  Per key tile j:
@@ -444,6 +440,7 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
       const uint32_t kslot = ring_iter % kSlots;
       if (!(ok = wait_bar(bar_at(sm, B_RING_FULL + kslot), (ring_iter / kSlots) & 1, err, E_MMA_K_FULL))) break;
       if (j == 0 && !(ok = wait_bar(bar_at(sm, B_Q_FULL), unit_iter & 1, err, E_MMA_Q_FULL))) break;
+      fence_proxy_async();  // rows landed by cp.async -> visible to the tensor core
       tc_fence_after();
       const uint32_t kt = sm.ring + kslot * kTileBytes;
 #pragma unroll
@@ -472,6 +469,7 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
       if (!(ok = wait_bar(bar_at(sm, B_RING_FULL + vslot), (ring_iter / kSlots) & 1, err, E_MMA_V_FULL))) break;
       if (!(ok = wait_bar(bar_at(sm, B_P_FULL + 0), p_cnt0 & 1, err, E_MMA_P0))) break;
       ++p_cnt0;
+      fence_proxy_async();
       tc_fence_after();
       const uint32_t vt = sm.ring + vslot * kTileBytes;
 #pragma unroll
@@ -667,10 +665,10 @@ __global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(bar_at(sm, B_RING_FULL + s), kLoaderWarps);
+      mbar_init(bar_at(sm, B_RING_FULL + s), 32 * kLoaderWarps);
       mbar_init(bar_at(sm, B_RING_EMPTY + s), 1);
     }
-    mbar_init(bar_at(sm, B_Q_FULL), kLoaderWarps);
+    mbar_init(bar_at(sm, B_Q_FULL), 32 * kLoaderWarps);
     mbar_init(bar_at(sm, B_Q_EMPTY), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_at(sm, B_S_FULL + t), 1);
@@ -695,7 +693,6 @@ __global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
     softmax_role(prm, sm, tmem, warp, lane);
   } else if (warp < kMmaWarp) {
     loader_role(prm, sm, warp - kLoaderWarp0, lane);
-    cp_async_wait_all();
   } else if (lane == 0) {
     mma_role(prm, sm, tmem);
   }
