@@ -31,6 +31,19 @@ sys.path.insert(0, ROOT)
 METRIC = "window-attention TFLOP/s per step (regular + shifted layer, transition included)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM bytes (read + write) of one regular-layout attention launch of the
+# 24-head 720p workload: an ncu capture of the same grid with 8 heads measured
+# 886.4 MB, scaled x3 (each head's rows are disjoint, so traffic grows with the
+# head count).  Valid only for the kernel source it was measured on.
+MEASURED_TRAFFIC = {"kernel_sha1": "605d60815dd60c64", "workload": "720p", "heads": 24, "bytes": 2.659e9}
+
+
+def kernel_sha1():
+    import hashlib
+    path = os.path.join(ROOT, "shifted_window_attention_gb300", "csrc", "attention_tc.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:16]
+
 
 def attn_flops(offsets, heads, d):
     n = np.diff(np.asarray(offsets, dtype=np.float64))
@@ -43,6 +56,23 @@ def load_peaks():
         with open(path) as f:
             return json.load(f), "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The largest `value` over all ranks (the slowest rank sets a step's
+    time); the value itself when not distributed."""
+    import torch
+    if dist is None or not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step, ms_per_step, world_size):
+    """Aggregate throughput: every rank processes the same per-step work
+    (weak scaling), in the time of the slowest rank."""
+    return world_size * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
 def dist_env():
@@ -179,10 +209,7 @@ def run_ours(args):
     a_r = [e[0].elapsed_time(e[1]) for e in ev]
     t_x = [e[1].elapsed_time(e[2]) for e in ev]
     a_s = [e[2].elapsed_time(e[3]) for e in ev]
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist if ws > 1 else None, dev)
     ms_step = total_ms / args.steps
 
     # End to end through the public API with pinned host buffers: H2D of this
@@ -218,14 +245,11 @@ def run_ours(args):
     ee.record(stream)
     torch.cuda.synchronize()
     e2e_ms = es.elapsed_time(ee) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist if ws > 1 else None, dev)
     if reg.device_status() or sft.device_status():
         raise RuntimeError("device error during the timed region")
 
-    e2e = {"value": round(ws * (fl_r + fl_s) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    e2e = {"value": round(whole_job_tflops(fl_r + fl_s, e2e_ms, ws), 2), "unit": "TFLOP/s",
            "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
     return finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, ms_step, e2e,
                   trans_bytes, clk, plan_ms, N, dist)
@@ -234,10 +258,16 @@ def run_ours(args):
 def finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, ms_step, e2e,
            trans_bytes, clk, plan_ms, N, dist):
     peaks, peak_kind = load_peaks()
+    traffic, traffic_note = None, "no ncu capture for this kernel source / workload"
+    mt = MEASURED_TRAFFIC
+    if kernel_sha1() == mt["kernel_sha1"] and wl.name == mt["workload"] and wl.heads == mt["heads"]:
+        traffic = mt["bytes"]
+        traffic_note = ("DRAM bytes of the regular-layout launch (ncu capture of the 8-head case scaled x3); "
+                        f"algorithmic {4.0 * N * wl.channels * 2:.3e} B")
     attn_ms = (np.mean(a_r) + np.mean(a_s)) / 2
     fl_launch = (fl_r + fl_s) / 2
     achieved = fl_launch / (attn_ms * 1e-3) / 1e12
-    value = ws * (fl_r + fl_s) / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(fl_r + fl_s, ms_step, ws)
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -276,7 +306,8 @@ def finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, 
             "frac": round(achieved / peaks["bf16_tflops"], 4),
             "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
             "peak_source": f"{peak_kind} bf16 burst",
-            "traffic": None,
+            "traffic": traffic,
+            "traffic_note": traffic_note,
         },
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
