@@ -17,7 +17,8 @@
 //  * Warp roles: warps 0-3 run the softmax of Q tile 0 and warps 4-7 that of
 //    Q tile 1 (one query row per thread = one TMEM lane); warps 8-9 gather
 //    Q/K/V rows with 16-byte cp.async into 128B-swizzled shared-memory tiles;
-//    one thread of warp 10 issues every tcgen05.mma.
+//    one thread of warp 10 issues every tcgen05.mma, and one thread of warp 11
+//    takes work units from the global counter up to two units ahead.
 //  * TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The bf16
 //    probabilities P overwrite the first 64 columns of their S tile and feed
 //    the P V product straight from TMEM (A operand in TMEM); V is the B
@@ -27,6 +28,8 @@
 //    2^8, which keeps every probability <= 256 and the result exact up to
 //    rounding.  The row sum accumulates the same bf16-rounded probabilities
 //    that enter the P V product.
+//  * Output rows leave TMEM through registers with 256-bit stores when the
+//    output is 32-byte aligned.
 //  * Every wait is bounded: after ~1 s a wait records an error code in the
 //    plan's workspace and the CTA unwinds, drains its MMAs and cp.asyncs and
 //    frees TMEM.
@@ -50,7 +53,8 @@ constexpr int kLoaderWarp0 = 8;
 constexpr int kLoaderWarps = 2;
 constexpr int kLoaderRows = kTile / kLoaderWarps;  // 64 rows of each tile per gather warp
 constexpr int kMmaWarp = kLoaderWarp0 + kLoaderWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;       // 11 warps: at most 3 per SM sub-partition
+constexpr int kSchedWarp = kMmaWarp + 1;
+constexpr int kThreads = (kSchedWarp + 1) * 32;     // 12 warps: 3 per SM sub-partition
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 
@@ -87,7 +91,7 @@ constexpr uint32_t kIdescPV = kIdescS | (1u << 16);
 
 // Error codes recorded in the workspace error word (which wait gave up).
 enum : int {
-  E_LOAD_UNIT_EMPTY = 0x101, E_LOAD_UNIT_FULL, E_LOAD_Q_EMPTY, E_LOAD_RING_EMPTY,
+  E_LOAD_UNIT_EMPTY = 0x101, E_LOAD_UNIT_FULL, E_LOAD_Q_EMPTY, E_LOAD_RING_EMPTY, E_SCHED_UNIT_EMPTY,
   E_MMA_UNIT_FULL = 0x201, E_MMA_Q_FULL, E_MMA_K_FULL, E_MMA_V_FULL, E_MMA_P0, E_MMA_P1, E_MMA_DRAIN,
   E_SM_UNIT_FULL = 0x301, E_SM_S_FULL, E_SM_O_FULL
 };
@@ -104,6 +108,7 @@ struct TcParams {
   int heads;
   long long row_stride;  // bytes between consecutive tokens (heads * 256)
   float c;               // softmax scale * log2(e)
+  int o_v8;              // output rows 32-byte aligned: 256-bit stores
   int* work;             // workspace words
 };
 
@@ -367,22 +372,6 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
   while (true) {
     const int us = unit_iter & 1;
     const uint32_t uph = (unit_iter >> 1) & 1;
-    if (lw == 0) {
-      // The first gather warp hands out the next unit to every role.
-      if (!acquire(bar_at(sm, B_UNIT_EMPTY + us), uph ^ 1, E_LOAD_UNIT_EMPTY)) break;
-      if (lane == 0) {
-        const int u = atomicAdd(prm.work + WS_NEXT_UNIT, 1);
-        int4 info = make_int4(0, -1, 0, 0);
-        if (u < prm.num_units) {
-          const WorkItem it = prm.items[u / prm.heads];
-          const int off = prm.offsets[it.window];
-          info = make_int4(off, prm.offsets[it.window + 1] - off, it.q_start, u % prm.heads);
-        }
-        sm.units[us] = info;
-        mbar_arrive(bar_at(sm, B_UNIT_FULL + us));
-      }
-      __syncwarp();
-    }
     if (!acquire(bar_at(sm, B_UNIT_FULL + us), uph, E_LOAD_UNIT_FULL)) break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
@@ -414,6 +403,27 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     ++unit_iter;
   }
   cp_async_wait_all();
+}
+
+// One thread hands out work units: it takes the next unit from the global
+// counter as soon as a unit slot is free, so the next unit's description is
+// ready (up to two units ahead) before the gather warps finish the current one.
+__device__ __forceinline__ void scheduler_role(const TcParams& prm, const Smem& sm) {
+  int* err = prm.work + WS_ERROR;
+  for (uint32_t unit_iter = 0;; ++unit_iter) {
+    const int us = unit_iter & 1;
+    if (!wait_bar(bar_at(sm, B_UNIT_EMPTY + us), ((unit_iter >> 1) & 1) ^ 1, err, E_SCHED_UNIT_EMPTY)) break;
+    const int u = atomicAdd(prm.work + WS_NEXT_UNIT, 1);
+    int4 info = make_int4(0, -1, 0, 0);
+    if (u < prm.num_units) {
+      const WorkItem it = prm.items[u / prm.heads];
+      const int off = prm.offsets[it.window];
+      info = make_int4(off, prm.offsets[it.window + 1] - off, it.q_start, u % prm.heads);
+    }
+    sm.units[us] = info;
+    mbar_arrive(bar_at(sm, B_UNIT_FULL + us));
+    if (info.y < 0) break;
+  }
 }
 
 // One thread issues every MMA.  Per key tile j:
@@ -496,6 +506,14 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
   // Drain: every MMA issued so far must finish before TMEM is freed.
   tc_commit(bar_at(sm, B_DRAIN));
   wait_bar(bar_at(sm, B_DRAIN), 0, err, E_MMA_DRAIN);
+}
+
+// 32 bytes in one store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+               "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -636,8 +654,16 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
 #pragma unroll
         for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(x[2 * i] * inv, x[2 * i + 1] * inv);
         if (valid) {
+          if (prm.o_v8) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) dst[8 * h + k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            for (int k = 0; k < 4; ++k)
+              st_global_v8(dst + 8 * h + 2 * k, pk[8 * k], pk[8 * k + 1], pk[8 * k + 2], pk[8 * k + 3], pk[8 * k + 4],
+                           pk[8 * k + 5], pk[8 * k + 6], pk[8 * k + 7]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[8 * h + k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
         }
       }
       tc_fence_before();
@@ -693,8 +719,10 @@ __global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
     softmax_role(prm, sm, tmem, warp, lane);
   } else if (warp < kMmaWarp) {
     loader_role(prm, sm, warp - kLoaderWarp0, lane);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_role(prm, sm, tmem);
   } else if (lane == 0) {
-    mma_role(prm, sm, tmem);
+    scheduler_role(prm, sm);
   }
 
   tc_fence_before();
@@ -732,6 +760,7 @@ cudaError_t launch_attention_bf16_tc(const wsa_plan_s& p, const void* q, const v
   prm.heads = heads;
   prm.row_stride = static_cast<long long>(heads) * kD * 2;
   prm.c = scale * 1.4426950408889634f;
+  prm.o_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 && (prm.row_stride & 31) == 0;
   prm.work = p.d_work;
   cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
