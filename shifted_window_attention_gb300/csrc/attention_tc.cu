@@ -48,7 +48,7 @@ constexpr int kD = 128;                     // head dim
 constexpr int kTile = 128;                  // rows of a Q / K / V tile
 constexpr int kTileBytes = kTile * kD * 2;  // 32 KB
 constexpr int kPanelBytes = kTile * 128;    // 128 rows x 128 B (64 channels), one swizzle panel
-constexpr int kSlots = 4;                   // K/V ring slots
+constexpr int kSlots = 5;                   // K/V ring slots
 constexpr int kLoaderWarp0 = 8;
 constexpr int kLoaderWarps = 2;
 constexpr int kLoaderRows = kTile / kLoaderWarps;  // 64 rows of each tile per gather warp
