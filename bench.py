@@ -33,9 +33,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) of one regular-layout attention launch of the
 # 24-head 720p workload: an ncu capture of the same grid with 8 heads measured
-# 886.4 MB, scaled x3 (each head's rows are disjoint, so traffic grows with the
+# 884.9 MB, scaled x3 (each head's rows are disjoint, so traffic grows with the
 # head count).  Valid only for the kernel source it was measured on.
-MEASURED_TRAFFIC = {"kernel_sha1": "605d60815dd60c64", "workload": "720p", "heads": 24, "bytes": 2.659e9}
+MEASURED_TRAFFIC = {"kernel_sha1": "b5473f6a6dfaaa3f", "workload": "720p", "heads": 24, "bytes": 2.655e9}
 
 
 def kernel_sha1():
@@ -147,47 +147,47 @@ def run_ours(args):
     if args.heads:
         # same grid, fewer heads: the small case used for detailed profiles
         wl = wsa_inputs.Workload(f"{wl.name}-{args.heads}h", wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw,
-                                 args.heads, wl.head_dim, wl.dtype, wl.dist)
+                                 args.heads, wl.head_dim, wl.dtype, wl.dist, wl.layers)
     g = (wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw)
-    N, C = wl.num_tokens, wl.channels
+    N, C, L = wl.num_tokens, wl.channels, wl.layers
 
     t0 = time.perf_counter()
-    reg = wsa.Plan(*g, wsa.REGULAR)
-    sft = wsa.Plan(*g, wsa.SHIFTED)
+    plans = [wsa.Plan(*g, wsa.REGULAR), wsa.Plan(*g, wsa.SHIFTED)]
     torch.cuda.synchronize()
     plan_ms = (time.perf_counter() - t0) * 1e3
 
-    # Inputs: layer 0 (regular) and layer 1 (shifted) Q/K/V, hidden state rows.
-    q0, k0, v0 = wsa_inputs.qkv(wl, layer=0, device=dev)
-    q1, k1, v1 = wsa_inputs.qkv(wl, layer=1, device=dev)
-    x = wsa_inputs.activation(wl, device=dev)
-    o0 = torch.empty_like(q0)
-    o1 = torch.empty_like(q1)
-    y = torch.empty_like(x)
+    # Layer schedule: layout of layer l is regular for even l, shifted for odd
+    # l; a transition of the hidden state [N, C] runs between consecutive
+    # layers (L - 1 of them).  Inputs: seeded Q/K/V per layer; schedules longer
+    # than 4 layers cycle 4 seeded input sets (the values do not change the work).
+    n_sets = min(L, 4)
+    sets = [wsa_inputs.qkv(wl, layer=i, device=dev) for i in range(n_sets)]
+    outs = [torch.empty_like(sets[i % n_sets][0]) for i in range(min(L, 2))]
+    hidden = [wsa_inputs.activation(wl, device=dev), None]
+    hidden[1] = torch.empty_like(hidden[0])
     stream = torch.cuda.current_stream()
 
-    offs_r = reg.tables()[0].cpu().numpy()
-    offs_s = sft.tables()[0].cpu().numpy()
-    fl_r = attn_flops(offs_r, wl.heads, wl.head_dim)
-    fl_s = attn_flops(offs_s, wl.heads, wl.head_dim)
+    flops = [attn_flops(p.tables()[0].cpu().numpy(), wl.heads, wl.head_dim) for p in plans]
+    fl_step = sum(flops[l % 2] for l in range(L))
     trans_bytes = 2.0 * N * C * 2 + 2 * 4.0 * N  # read + write rows, two int32 table reads
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    n_ev = 2 * L
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
 
     def step(i=None):
         e = ev[i] if i is not None else None
-        if e: e[0].record(stream)
-        wsa.attention(reg, q0, k0, v0, out=o0)
-        if e: e[1].record(stream)
-        wsa.transition(reg, sft, x, out=y)
-        if e: e[2].record(stream)
-        wsa.attention(sft, q1, k1, v1, out=o1)
-        if e: e[3].record(stream)
+        for l in range(L):
+            q, k, v = sets[l % n_sets]
+            if e: e[2 * l].record(stream)
+            wsa.attention(plans[l % 2], q, k, v, out=outs[l % 2])
+            if e: e[2 * l + 1].record(stream)
+            if l + 1 < L:
+                wsa.transition(plans[l % 2], plans[(l + 1) % 2], hidden[l % 2], out=hidden[(l + 1) % 2])
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if reg.device_status() or sft.device_status():
+    if any(p.device_status() for p in plans):
         raise RuntimeError("device error during warm-up")
 
     clocks = ClockSampler(local)
@@ -206,57 +206,51 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
-    a_r = [e[0].elapsed_time(e[1]) for e in ev]
-    t_x = [e[1].elapsed_time(e[2]) for e in ev]
-    a_s = [e[2].elapsed_time(e[3]) for e in ev]
+    attn = np.array([[e[2 * l].elapsed_time(e[2 * l + 1]) for l in range(L)] for e in ev])  # [steps, L]
+    trans = np.array([[e[2 * l + 1].elapsed_time(e[2 * l + 2]) for l in range(L - 1)] for e in ev])
     total_ms = max_over_ranks(total_ms, dist if ws > 1 else None, dev)
     ms_step = total_ms / args.steps
-
-    # End to end through the public API with pinned host buffers: H2D of this
-    # step's Q/K/V (both layers) and hidden rows, the three calls, D2H of the
-    # two attention outputs and the transitioned rows.
-    if args.no_e2e:
-        return finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, ms_step, None,
-                      trans_bytes, clk, plan_ms, N, dist)
-    host_in = [t.cpu().pin_memory() for t in (q0, k0, v0, q1, k1, v1, x)]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o0, o1, y)]
-    dev_in = [q0, k0, v0, q1, k1, v1, x]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
-    e2e_steps = max(1, min(args.steps, 5))
-
-    def e2e_step():
-        for d_, h_ in zip(dev_in, host_in):
-            d_.copy_(h_, non_blocking=True)
-        wsa.attention(reg, q0, k0, v0, out=o0)
-        wsa.transition(reg, sft, x, out=y)
-        wsa.attention(sft, q1, k1, v1, out=o1)
-        for h_, d_ in zip(host_out, (o0, o1, y)):
-            h_.copy_(d_, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    es.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    ee.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = es.elapsed_time(ee) / e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, dist if ws > 1 else None, dev)
-    if reg.device_status() or sft.device_status():
+    if any(p.device_status() for p in plans):
         raise RuntimeError("device error during the timed region")
 
-    e2e = {"value": round(whole_job_tflops(fl_r + fl_s, e2e_ms, ws), 2), "unit": "TFLOP/s",
-           "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
-    return finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, ms_step, e2e,
-                  trans_bytes, clk, plan_ms, N, dist)
+    # End to end through the public API with pinned host buffers (two-layer
+    # workloads): H2D of this step's Q/K/V of both layers and the hidden rows,
+    # the three calls, D2H of the two attention outputs and the transitioned rows.
+    e2e = None
+    if L == 2 and not args.no_e2e:
+        q0, k0, v0 = sets[0]
+        q1, k1, v1 = sets[1]
+        x, y = hidden
+        dev_in = [q0, k0, v0, q1, k1, v1, x]
+        host_in = [t.cpu().pin_memory() for t in dev_in]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (outs[0], outs[1], y)]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        e2e_steps = max(1, min(args.steps, 5))
 
+        def e2e_step():
+            for d_, h_ in zip(dev_in, host_in):
+                d_.copy_(h_, non_blocking=True)
+            wsa.attention(plans[0], q0, k0, v0, out=outs[0])
+            wsa.transition(plans[0], plans[1], x, out=y)
+            wsa.attention(plans[1], q1, k1, v1, out=outs[1])
+            for h_, d_ in zip(host_out, (outs[0], outs[1], y)):
+                h_.copy_(d_, non_blocking=True)
 
-def finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, ms_step, e2e,
-           trans_bytes, clk, plan_ms, N, dist):
+        e2e_step()
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(es.elapsed_time(ee) / e2e_steps, dist if ws > 1 else None, dev)
+        e2e = {"value": round(whole_job_tflops(fl_step, e2e_ms, ws), 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
     peaks, peak_kind = load_peaks()
     traffic, traffic_note = None, "no ncu capture for this kernel source / workload"
     mt = MEASURED_TRAFFIC
@@ -264,13 +258,29 @@ def finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, 
         traffic = mt["bytes"]
         traffic_note = ("DRAM bytes of the regular-layout launch (ncu capture of the 8-head case scaled x3); "
                         f"algorithmic {4.0 * N * wl.channels * 2:.3e} B")
-    attn_ms = (np.mean(a_r) + np.mean(a_s)) / 2
-    fl_launch = (fl_r + fl_s) / 2
+    a_reg = attn[:, 0::2].mean()
+    a_sft = attn[:, 1::2].mean() if L > 1 else float("nan")
+    attn_ms = attn.mean()
+    fl_launch = fl_step / L
     achieved = fl_launch / (attn_ms * 1e-3) / 1e12
-    value = whole_job_tflops(fl_r + fl_s, ms_step, ws)
+    t_mean = float(trans.mean()) if L > 1 else float("nan")
+    per_layer = {
+        "attention_ms": [round(float(a_reg), 4), round(float(a_sft), 4)],
+        "attention_tflops": [round(flops[0] / (a_reg * 1e9), 1), round(flops[1] / (a_sft * 1e9), 1)],
+        "tokens_per_s": [round(N / (a_reg * 1e-3)), round(N / (a_sft * 1e-3))],
+        "transition_ms": round(t_mean, 4),
+        "transition_gbs": round(trans_bytes / (t_mean * 1e6), 1),
+        "transition_frac_hbm": round(trans_bytes / (t_mean * 1e6) / peaks["hbm_gbs"], 4),
+        "plan_build_ms_host_incl": round(plan_ms, 3),
+    }
+    if L > 2:
+        per_layer["attention_ms_by_layer"] = [round(float(x), 4) for x in attn.mean(axis=0)]
+        per_layer["transition_ms_by_boundary"] = [round(float(x), 4) for x in trans.mean(axis=0)]
+    dist_note = {"normal": "N(0,1)", "normal_half_var": "N(0,1)/sqrt(2)",
+                 "outlier": "Q,K N(0,1) with 1% of channels x8, V N(0,1)"}[wl.dist]
     result = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": round(whole_job_tflops(fl_step, ms_step, ws), 2),
         "unit": "TFLOP/s",
         "n_gpus": ws,
         "steps": args.steps,
@@ -280,23 +290,16 @@ def finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, 
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded torch.randn, N(0,1)/sqrt(2), bf16)",
+        "data": f"synthetic (seeded torch.randn, {dist_note}, bf16)",
         "config": {"workload": f"{wl.name}: T={wl.T},H={wl.H},W={wl.W} ({N} tokens), nt,nh,nw={wl.nt},{wl.nh},{wl.nw} "
-                               f"-> wt,wh,ww={reg.wt},{reg.wh},{reg.ww}; {wl.heads} heads x {wl.head_dim}; "
-                               "regular attn + transition [N,3072] + shifted attn",
-                   "tokens": N, "heads": wl.heads, "head_dim": wl.head_dim,
-                   "windows": [reg.num_windows, sft.num_windows],
-                   "l2": "inputs larger than L2 (Q/K/V 464 MB each); no flush",
+                               f"-> wt,wh,ww={plans[0].wt},{plans[0].wh},{plans[0].ww}; {wl.heads} heads x {wl.head_dim}; "
+                               f"{L} alternating layers (attention gathers/scatters through ids) with "
+                               f"{L - 1} transitions of [N,{C}]",
+                   "tokens": N, "heads": wl.heads, "head_dim": wl.head_dim, "layers": L,
+                   "windows": [plans[0].num_windows, plans[1].num_windows],
+                   "l2": "inputs larger than L2 (Q/K/V >= 155 MB each); no flush",
                    "parallelism": "replicas" if ws > 1 else "single"},
-        "per_layer": {
-            "attention_ms": [round(float(np.mean(a_r)), 4), round(float(np.mean(a_s)), 4)],
-            "attention_tflops": [round(fl_r / (np.mean(a_r) * 1e9), 1), round(fl_s / (np.mean(a_s) * 1e9), 1)],
-            "tokens_per_s": [round(N / (np.mean(a_r) * 1e-3)), round(N / (np.mean(a_s) * 1e-3))],
-            "transition_ms": round(float(np.mean(t_x)), 4),
-            "transition_gbs": round(trans_bytes / (np.mean(t_x) * 1e6), 1),
-            "transition_frac_hbm": round(trans_bytes / (np.mean(t_x) * 1e6) / peaks["hbm_gbs"], 4),
-            "plan_build_ms_host_incl": round(plan_ms, 3),
-        },
+        "per_layer": per_layer,
         "roofline": {
             "bound": "tensor",
             "kernel": "attention_tc_kernel",
@@ -310,10 +313,11 @@ def finish(args, ws, rank, wl, reg, sft, q0, k0, v0, fl_r, fl_s, a_r, a_s, t_x, 
             "traffic_note": traffic_note,
         },
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (2 * L - 1) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
+        q0, k0, v0 = sets[0]
         result["cpu_baseline"] = cpu_baseline(wl, tuple(t.float().cpu().numpy() for t in (q0, k0, v0)),
                                               seconds=args.cpu_seconds)
     if ws > 1:
