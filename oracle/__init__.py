@@ -23,7 +23,8 @@ grids and library routines; none is "parity unpinned".
 from .geometry import window_size, axis_intervals, windows, WINDOW_REF_AREA
 from .plan import Plan, make_plan, cu_seqlens
 from .transition import transition, gather_table
-from .attention import window_attention, masked_full_attention, window_attention_rows
+from .attention import (window_attention, masked_full_attention, window_attention_rows,
+                        window_attention_text)
 from .planner import lpt_assign
 
 __all__ = [
@@ -39,5 +40,6 @@ __all__ = [
     "window_attention",
     "window_attention_rows",
     "masked_full_attention",
+    "window_attention_text",
     "lpt_assign",
 ]

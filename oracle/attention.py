@@ -89,3 +89,36 @@ def masked_full_attention(q, k, v, plan, scale=None, canonical=True):
         s = np.where(same, s, -np.inf)
         out[:, h, :] = _softmax_rows(s) @ v[:, h, :]
     return out
+
+
+def window_attention_text(q, k, v, q_txt, k_txt, v_txt, plan, scale=None, canonical=True):
+    """Window attention over packed segments [video window, replicated text].
+
+    "Window-Aligned Sequence Parallelism (SeedVR2)", sections "SeedVR2
+    integration" and "Text stream": every window's attention is one segment
+    made of the window's video tokens followed by the text tokens (the same
+    text for every window); each window yields a text output, and the layer's
+    text output is the sum of the per-window text outputs divided by the
+    global window count of the layout:  T = (sum_w T_w) / W.
+
+    q, k, v: [N, heads, d] (canonical or packed rows); q_txt, k_txt, v_txt:
+    [n_text, heads, d].  Returns (video output [N, heads, d], text output
+    [n_text, heads, d]), both fp64."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    qt, kt, vt = _as64(q_txt), _as64(k_txt), _as64(v_txt)
+    n_tok, heads, d = q.shape
+    n_text = qt.shape[0]
+    c = _scale(d, scale)
+    out = np.empty_like(q)
+    t_sum = np.zeros((n_text, heads, d))
+    for w in range(plan.num_windows):
+        rows = _rows_of_window(plan, w, canonical)
+        n = rows.size
+        for h in range(heads):
+            qs = np.concatenate([q[rows, h, :], qt[:, h, :]])
+            ks = np.concatenate([k[rows, h, :], kt[:, h, :]])
+            vs = np.concatenate([v[rows, h, :], vt[:, h, :]])
+            o = _softmax_rows((qs @ ks.T) * c) @ vs
+            out[rows, h, :] = o[:n]
+            t_sum[:, h, :] += o[n:]
+    return out, t_sum / plan.num_windows
