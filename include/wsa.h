@@ -23,6 +23,8 @@
 #ifndef WSA_H_
 #define WSA_H_
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -127,6 +129,36 @@ wsa_status wsa_attention(wsa_plan_t plan, const void* q, const void* k,
                          const void* v, void* o, int heads, int head_dim,
                          wsa_dtype dtype, int in_order_canonical,
                          float softmax_scale, void* stream);
+
+/*
+ * wsa_attention_text -- window attention over packed segments
+ * [video window, replicated text] with the text output averaged over windows.
+ * "Window-Aligned Sequence Parallelism (SeedVR2)", sections "SeedVR2
+ * integration" (window attention is a packed call over [video window,
+ * replicated text] segments) and "Text stream" (each window yields a text
+ * output; the layer's text output is their sum divided by the global window
+ * count, T = (sum_w T_w) / W, not a token-weighted mean).
+ *
+ * For window w and head h the segment is S_w = [video rows of w ; the n_text
+ * text rows]; O_seg = softmax(Q_seg K_seg^T * scale) V_seg.  Video rows of O
+ * go to `o` (layout of wsa_attention); text rows give T_w, and o_txt receives
+ * (sum_w T_w) / W, summed in window order (deterministic).
+ * q, k, v, o: [N, heads, 128] bf16 (canonical or packed rows as in
+ * wsa_attention); q_txt, k_txt, v_txt, o_txt: [n_text, heads, 128] bf16.
+ * workspace: device, 256-byte aligned, at least wsa_attention_text_workspace
+ * bytes (the work list and W x n_text x heads x 128 fp32 partials); owned by
+ * the caller, contents undefined after the call.  n_text > 0; bf16 and
+ * head_dim 128 only (WSA_ERR_UNSUPPORTED otherwise); at most 65535 heads and
+ * 65535 windows.  Outputs and workspace must not overlap inputs.
+ */
+wsa_status wsa_attention_text_workspace(wsa_plan_t plan, int n_text, int heads,
+                                        int head_dim, wsa_dtype dtype, size_t* bytes);
+wsa_status wsa_attention_text(wsa_plan_t plan, const void* q, const void* k,
+                              const void* v, void* o, const void* q_txt,
+                              const void* k_txt, const void* v_txt, void* o_txt,
+                              int n_text, int heads, int head_dim, wsa_dtype dtype,
+                              int in_order_canonical, float softmax_scale,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * wsa_transition -- the local-permutation layout change between layers.

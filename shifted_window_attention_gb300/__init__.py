@@ -57,6 +57,8 @@ def _load():
         "wsa_transition": ([p, p, p, p, i, i, p], i),
         "wsa_plan_device_status": ([p, ip], i),
         "wsa_attention_noalloc": ([i] * 8 + [p, p, p, p, i, i, f, p], i),
+        "wsa_attention_text_workspace": ([p, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)], i),
+        "wsa_attention_text": ([p] + [p] * 8 + [i, i, i, i, i, f, p, ctypes.c_size_t, p], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -193,6 +195,38 @@ def attention(plan, q, k, v, out=None, canonical=True, scale=0.0, stream=None):
     return out
 
 
+def attention_text_workspace_bytes(plan, n_text, heads):
+    n = ctypes.c_size_t()
+    _check(lib.wsa_attention_text_workspace(plan.handle, n_text, heads, 128, BF16, ctypes.byref(n)))
+    return n.value
+
+
+def attention_text(plan, q, k, v, q_txt, k_txt, v_txt, out=None, out_txt=None, canonical=True, scale=0.0,
+                   workspace=None, stream=None):
+    """Window attention over [video window, replicated text] segments.
+
+    Returns (video output like q, text output like q_txt): the text output is
+    the mean over windows of each window's text rows.  bf16, head_dim 128."""
+    for t in (q, k, v, q_txt, k_txt, v_txt):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 3 or t.dtype != torch.bfloat16:
+            raise WsaError(-1, "tensors must be contiguous 3-D bf16 CUDA tensors")
+    if k.shape != q.shape or v.shape != q.shape or q.shape[0] != plan.num_tokens:
+        raise WsaError(-1, "q, k, v must be [N, heads, 128] for the plan")
+    if k_txt.shape != q_txt.shape or v_txt.shape != q_txt.shape or q_txt.shape[1:] != q.shape[1:]:
+        raise WsaError(-1, "text tensors must be [n_text, heads, 128]")
+    n_text, heads = q_txt.shape[0], q.shape[1]
+    out = torch.empty_like(q) if out is None else out
+    out_txt = torch.empty_like(q_txt) if out_txt is None else out_txt
+    need = attention_text_workspace_bytes(plan, n_text, heads)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(lib.wsa_attention_text(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(q_txt), _ptr(k_txt),
+                                  _ptr(v_txt), _ptr(out_txt), n_text, heads, 128, BF16, 1 if canonical else 0,
+                                  float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+    return out, out_txt
+
+
 def transition(src, dst, x, out=None, stream=None):
     """Rows of x (packed order of plan ``src``) rearranged into the packed order
     of plan ``dst``: out[p] = x[pos_src[ids_dst[p]]]."""
@@ -227,5 +261,6 @@ def attention_noalloc(T, H, W, nt, nh, nw, layout, q, k, v, out, canonical=True,
 
 __all__ = [
     "REGULAR", "SHIFTED", "BF16", "FP32", "WsaError", "Plan", "attention", "transition",
-    "window_size", "layout_windows", "version", "lib", "attention_noalloc",
+    "window_size", "layout_windows", "version", "lib", "attention_noalloc", "attention_text",
+    "attention_text_workspace_bytes",
 ]

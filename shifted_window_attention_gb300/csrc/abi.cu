@@ -44,6 +44,8 @@ wsa_status wsa_attention(wsa_plan_t plan, const void* q, const void* k, const vo
     return fail(WSA_ERR_INVALID_ARG, "o must not overlap q, k or v");
   if (static_cast<long long>(plan->num_tc_items) * heads >= (1LL << 31))
     return fail(WSA_ERR_UNSUPPORTED, "too many work units (windows x heads)");
+  if (dtype == WSA_BF16 && (heads > 65535 || plan->num_windows > 65535))
+    return fail(WSA_ERR_UNSUPPORTED, "bf16 attention supports at most 65535 heads and 65535 windows");
   if (heads > 65535 && dtype == WSA_FP32)
     return fail(WSA_ERR_UNSUPPORTED, "fp32 attention supports at most 65535 heads");
   int dev = -1;
@@ -61,6 +63,64 @@ wsa_status wsa_attention(wsa_plan_t plan, const void* q, const void* k, const vo
     e = launch_attention_bf16_tc(*plan, q, k, v, o, heads, in_order_canonical == 1, scale, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "wsa_attention: launch");
+  return WSA_OK;
+}
+
+wsa_status wsa_attention_text_workspace(wsa_plan_t plan, int n_text, int heads, int head_dim, wsa_dtype dtype,
+                                        size_t* bytes) {
+  if (!plan || !bytes) return fail(WSA_ERR_INVALID_ARG, "plan and bytes must be non-null");
+  if (n_text <= 0 || heads <= 0) return fail(WSA_ERR_INVALID_ARG, "n_text and heads must be > 0");
+  if (dtype != WSA_BF16 || head_dim != 128)
+    return fail(WSA_ERR_UNSUPPORTED, "the text segment is implemented for bf16, head_dim 128");
+  *bytes = attention_text_workspace_bytes(*plan, n_text, heads, nullptr);
+  return WSA_OK;
+}
+
+wsa_status wsa_attention_text(wsa_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                              const void* q_txt, const void* k_txt, const void* v_txt, void* o_txt, int n_text,
+                              int heads, int head_dim, wsa_dtype dtype, int in_order_canonical, float softmax_scale,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan) return fail(WSA_ERR_INVALID_ARG, "plan is null");
+  if (!q || !k || !v || !o || !q_txt || !k_txt || !v_txt || !o_txt || !workspace)
+    return fail(WSA_ERR_INVALID_ARG, "tensors and workspace must be non-null");
+  if (n_text <= 0 || heads <= 0) return fail(WSA_ERR_INVALID_ARG, "n_text and heads must be > 0");
+  if (in_order_canonical != 0 && in_order_canonical != 1)
+    return fail(WSA_ERR_INVALID_ARG, "in_order_canonical must be 0 or 1");
+  if (!std::isfinite(softmax_scale)) return fail(WSA_ERR_INVALID_ARG, "softmax_scale is not finite");
+  if (dtype != WSA_BF16 || head_dim != 128)
+    return fail(WSA_ERR_UNSUPPORTED, "the text segment is implemented for bf16, head_dim 128");
+  if (heads > 65535 || plan->num_windows > 65535)
+    return fail(WSA_ERR_UNSUPPORTED, "at most 65535 heads and 65535 windows");
+  if (static_cast<long long>(plan->max_window_tokens) + n_text >= (1LL << 30))
+    return fail(WSA_ERR_UNSUPPORTED, "segment too long");
+  const void* ins[] = {q, k, v, q_txt, k_txt, v_txt, o, o_txt};
+  for (const void* ptr : ins)
+    if (!aligned16(ptr)) return fail(WSA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(WSA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = attention_text_workspace_bytes(*plan, n_text, heads, nullptr);
+  if (workspace_bytes < need)
+    return fail(WSA_ERR_INVALID_ARG, "workspace too small: need " + std::to_string(need) + " bytes");
+  const size_t vb = static_cast<size_t>(plan->num_tokens) * heads * head_dim * 2;
+  const size_t tb = static_cast<size_t>(n_text) * heads * head_dim * 2;
+  const void* inv[] = {q, k, v};
+  const void* int_[] = {q_txt, k_txt, v_txt};
+  for (const void* ptr : inv)
+    if (overlap(o, vb, ptr, vb) || overlap(o_txt, tb, ptr, vb) || overlap(workspace, need, ptr, vb))
+      return fail(WSA_ERR_INVALID_ARG, "outputs or workspace overlap an input");
+  for (const void* ptr : int_)
+    if (overlap(o, vb, ptr, tb) || overlap(o_txt, tb, ptr, tb) || overlap(workspace, need, ptr, tb))
+      return fail(WSA_ERR_INVALID_ARG, "outputs or workspace overlap an input");
+  if (overlap(o, vb, o_txt, tb) || overlap(workspace, need, o, vb) || overlap(workspace, need, o_txt, tb))
+    return fail(WSA_ERR_INVALID_ARG, "outputs and workspace must not overlap");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_attention_text: cudaGetDevice");
+  if (dev != plan->device) return fail(WSA_ERR_INVALID_ARG, "plan was created on another device");
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  e = launch_attention_text_bf16_tc(*plan, q, k, v, o, q_txt, k_txt, v_txt, o_txt, n_text, heads,
+                                    in_order_canonical == 1, scale, workspace, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_attention_text: launch");
   return WSA_OK;
 }
 

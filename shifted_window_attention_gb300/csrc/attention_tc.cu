@@ -106,6 +106,15 @@ struct TcParams {
   const WorkItem* items;
   int num_units;
   int heads;
+  // Text segment (n_text = 0: video only).  Window w's attention runs over the
+  // segment [its n_w video rows, the n_text text rows]; text query rows write
+  // fp32 partials T_w / W to text_part[w][t][head][128].
+  const char* qt;
+  const char* kt;
+  const char* vt;
+  float* text_part;
+  int n_text;
+  float inv_windows;
   long long row_stride;  // bytes between consecutive tokens (heads * 256)
   float c;               // softmax scale * log2(e)
   int o_v8;              // output rows 32-byte aligned: 256-bit stores
@@ -337,24 +346,27 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
   auto acquire = [&](uint32_t bar, uint32_t parity, int code) -> bool {
     return __all_sync(0xffffffffu, wait_bar(bar, parity, err, code));
   };
-  // lane l holds the ids of rows kLoaderRows*lw + l and + 32 + l of a tile
-  // starting at window row row0 (-1: past the window end)
-  auto fetch_ids = [&](int (&ids)[2], int row0, int n, int off) {
+  // lane l holds the row sources of segment rows kLoaderRows*lw + l and
+  // + 32 + l of a tile starting at segment row row0: id >= 0 is a video row,
+  // id <= -2 is text row -2 - id, -1 is past the segment end (zero fill).
+  auto fetch_ids = [&](int (&ids)[2], int row0, int nv, int n, int off) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int myrow = row0 + kLoaderRows * lw + 32 * h + lane;
       ids[h] = -1;
-      if (myrow < n) ids[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+      if (myrow < nv) ids[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+      else if (myrow < n) ids[h] = -2 - (myrow - nv);
     }
   };
-  auto copy_tile = [&](const char* src, uint32_t dst, const int (&ids)[2], int head) {
-    const char* colbase = src + static_cast<long long>(head) * (kD * 2) + chunk * 16;
+  auto copy_tile = [&](const char* src, const char* tsrc, uint32_t dst, const int (&ids)[2], int head) {
+    const long long col = static_cast<long long>(head) * (kD * 2) + chunk * 16;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const int r = kLoaderRows * lw + half + 2 * i;
       const int id = __shfl_sync(0xffffffffu, ids[i >> 4], half + 2 * (i & 15));
-      const char* g = id >= 0 ? colbase + static_cast<long long>(id) * prm.row_stride : src;
-      cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
+      const char* g = id >= 0 ? src + col + static_cast<long long>(id) * prm.row_stride
+                              : (id <= -2 ? tsrc + col + static_cast<long long>(-2 - id) * prm.row_stride : src);
+      cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id != -1 ? 16u : 0u);
     }
   };
   auto load_kv = [&](const int (&ids)[2], int head) -> bool {
@@ -362,7 +374,7 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
       const uint32_t slot = ring_iter % kSlots;
       if (!acquire(bar_at(sm, B_RING_EMPTY + slot), ((ring_iter / kSlots) & 1) ^ 1, E_LOAD_RING_EMPTY))
         return false;
-      copy_tile(which ? prm.v : prm.k, sm.ring + slot * kTileBytes, ids, head);
+      copy_tile(which ? prm.v : prm.k, which ? prm.vt : prm.kt, sm.ring + slot * kTileBytes, ids, head);
       cp_async_arrive(bar_at(sm, B_RING_FULL + slot));
       ++ring_iter;
     }
@@ -375,26 +387,26 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     if (!acquire(bar_at(sm, B_UNIT_FULL + us), uph, E_LOAD_UNIT_FULL)) break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int off = info.x, n = info.y, q0 = info.z, head = info.w;
+    const int off = info.x, nv = info.y, n = nv + prm.n_text, q0 = info.z, head = info.w & 0xffff;
     const int nkv = (n + kTile - 1) / kTile;
     const bool has1 = q0 + kTile < n;
     int ids[2], ids_next[2], qids0[2], qids1[2];
-    fetch_ids(ids, 0, n, off);
-    fetch_ids(qids0, q0, n, off);
-    if (has1) fetch_ids(qids1, q0 + kTile, n, off);
+    fetch_ids(ids, 0, nv, n, off);
+    fetch_ids(qids0, q0, nv, n, off);
+    if (has1) fetch_ids(qids1, q0 + kTile, nv, n, off);
     // K0/V0 first: they may land while the previous unit's last MMAs still
     // hold the Q buffers.
-    if (nkv > 1) fetch_ids(ids_next, kTile, n, off);
+    if (nkv > 1) fetch_ids(ids_next, kTile, nv, n, off);
     if (!load_kv(ids, head)) break;
     if (!acquire(bar_at(sm, B_Q_EMPTY), (unit_iter & 1) ^ 1, E_LOAD_Q_EMPTY)) break;
-    copy_tile(prm.q, sm.q0, qids0, head);
-    if (has1) copy_tile(prm.q, sm.q0 + kTileBytes, qids1, head);
+    copy_tile(prm.q, prm.qt, sm.q0, qids0, head);
+    if (has1) copy_tile(prm.q, prm.qt, sm.q0 + kTileBytes, qids1, head);
     cp_async_arrive(bar_at(sm, B_Q_FULL));
     bool ok = true;
     for (int j = 1; j < nkv && ok; ++j) {
       ids[0] = ids_next[0];
       ids[1] = ids_next[1];
-      if (j + 1 < nkv) fetch_ids(ids_next, (j + 1) * kTile, n, off);
+      if (j + 1 < nkv) fetch_ids(ids_next, (j + 1) * kTile, nv, n, off);
       ok = load_kv(ids, head);
     }
     if (!ok) break;
@@ -418,7 +430,7 @@ __device__ __forceinline__ void scheduler_role(const TcParams& prm, const Smem& 
     if (u < prm.num_units) {
       const WorkItem it = prm.items[u / prm.heads];
       const int off = prm.offsets[it.window];
-      info = make_int4(off, prm.offsets[it.window + 1] - off, it.q_start, u % prm.heads);
+      info = make_int4(off, prm.offsets[it.window + 1] - off, it.q_start, (u % prm.heads) | (it.window << 16));
     }
     sm.units[us] = info;
     mbar_arrive(bar_at(sm, B_UNIT_FULL + us));
@@ -441,7 +453,7 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
     if (!wait_bar(bar_at(sm, B_UNIT_FULL + us), (unit_iter >> 1) & 1, err, E_MMA_UNIT_FULL)) break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int n = info.y, q0 = info.z;
+    const int n = info.y + prm.n_text, q0 = info.z;
     const bool has1 = q0 + kTile < n;
     const int nkv = (n + kTile - 1) / kTile;
     bool ok = true;
@@ -615,7 +627,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
       break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int off = info.x, n = info.y, q0 = info.z, head = info.w;
+    const int off = info.x, nv = info.y, n = nv + prm.n_text, q0 = info.z, head = info.w & 0xffff;
     if (t == 0 || q0 + kTile < n) {
       const int nkv = (n + kTile - 1) / kTile;
       float m = -INFINITY;
@@ -641,15 +653,30 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
       tc_fence_after();
       const float inv = 1.f / ((la.x + la.y) + (lb.x + lb.y));
       const int qr = q0 + kTile * t + rq;
-      const bool valid = qr < n;
+      const bool valid = qr < nv;           // a video row of this window
+      const bool text = qr >= nv && qr < n;  // a text row: partial T_w / W
       long long tok = 0;
       if (valid) tok = prm.row_map ? __ldg(prm.row_map + off + qr) : off + qr;
+      float* tdst = nullptr;
+      if (text) {
+        const long long window = static_cast<unsigned>(info.w) >> 16;
+        tdst = prm.text_part + ((window * prm.n_text + (qr - nv)) * prm.heads + head) * kD;
+      }
       uint4* dst = reinterpret_cast<uint4*>(prm.o + tok * prm.row_stride + static_cast<long long>(head) * (kD * 2));
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float x[64];
         __syncwarp();
         tmem_ld64(tO + 64 * h, x);
+        if (text) {
+          const float sc = inv * prm.inv_windows;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            st_global_v8(tdst + 64 * h + 8 * k, __float_as_uint(x[8 * k] * sc), __float_as_uint(x[8 * k + 1] * sc),
+                         __float_as_uint(x[8 * k + 2] * sc), __float_as_uint(x[8 * k + 3] * sc),
+                         __float_as_uint(x[8 * k + 4] * sc), __float_as_uint(x[8 * k + 5] * sc),
+                         __float_as_uint(x[8 * k + 6] * sc), __float_as_uint(x[8 * k + 7] * sc));
+        }
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) pk[i] = pack_bf16(x[2 * i] * inv, x[2 * i + 1] * inv);
@@ -674,8 +701,8 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
   }
 }
 
-// Registers: each SM sub-partition holds 16K registers and at most 3 of the
-// 11 warps, so 168 registers per thread fit (3 x 32 x 168 = 16,128).
+// Registers: each SM sub-partition holds 16K registers and 3 of the 12
+// warps, so 168 registers per thread fit (3 x 32 x 168 = 16,128).
 __global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -746,8 +773,65 @@ __global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
 
 }  // namespace
 
+namespace {
+
+// Text output: o_txt[t][c] = sum over windows w of part[w][t][c] (each
+// partial already divided by the window count), summed in window order so
+// the result does not depend on scheduling; converted to bf16.
+__global__ void text_reduce_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ out, long long per_window,
+                                   int windows) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < per_window;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float acc = 0.f;
+    for (int w = 0; w < windows; ++w) acc += part[w * per_window + i];
+    out[i] = __float2bfloat16_rn(acc);
+  }
+}
+
+}  // namespace
+
+size_t attention_text_workspace_bytes(const wsa_plan_s& p, int n_text, int heads, size_t* items_bytes) {
+  std::vector<int> seg(p.h_offsets.size(), 0);
+  for (size_t w = 1; w < seg.size(); ++w) seg[w] = seg[w - 1] + (p.h_offsets[w] - p.h_offsets[w - 1]) + n_text;
+  const size_t n_items = make_items(seg, kTcItemRows, 128).size();
+  const size_t ib = (n_items * sizeof(WorkItem) + 255) / 256 * 256;
+  if (items_bytes) *items_bytes = ib;
+  return ib + static_cast<size_t>(p.num_windows) * n_text * heads * kD * sizeof(float);
+}
+
+cudaError_t launch_attention_text_bf16_tc(const wsa_plan_s& p, const void* q, const void* k, const void* v, void* o,
+                                          const void* qt, const void* kt, const void* vt, void* ot, int n_text,
+                                          int heads, bool canonical, float scale, void* workspace, cudaStream_t s) {
+  std::vector<int> seg(p.h_offsets.size(), 0);
+  for (size_t w = 1; w < seg.size(); ++w) seg[w] = seg[w - 1] + (p.h_offsets[w] - p.h_offsets[w - 1]) + n_text;
+  const std::vector<WorkItem> items = make_items(seg, kTcItemRows, 128);
+  size_t items_bytes = 0;
+  attention_text_workspace_bytes(p, n_text, heads, &items_bytes);
+  WorkItem* d_items = static_cast<WorkItem*>(workspace);
+  float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + items_bytes);
+  // pageable source: the copy stages the vector before returning
+  cudaError_t e = cudaMemcpyAsync(d_items, items.data(), items.size() * sizeof(WorkItem), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  e = launch_attention_tc(p, q, k, v, o, heads, canonical, scale, s, qt, kt, vt, part, n_text, d_items,
+                          static_cast<int>(items.size()));
+  if (e != cudaSuccess) return e;
+  const long long per_window = static_cast<long long>(n_text) * heads * kD;
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::min<long long>((per_window + threads - 1) / threads, 8LL * sm_count()));
+  text_reduce_kernel<<<std::max(1, blocks), threads, 0, s>>>(part, static_cast<__nv_bfloat16*>(ot), per_window,
+                                                              p.num_windows);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attention_bf16_tc(const wsa_plan_s& p, const void* q, const void* k, const void* v, void* o,
                                      int heads, bool canonical, float scale, cudaStream_t s) {
+  return launch_attention_tc(p, q, k, v, o, heads, canonical, scale, s, nullptr, nullptr, nullptr, nullptr, 0,
+                             p.d_tc_items, p.num_tc_items);
+}
+
+cudaError_t launch_attention_tc(const wsa_plan_s& p, const void* q, const void* k, const void* v, void* o, int heads,
+                                bool canonical, float scale, cudaStream_t s, const void* qt, const void* kt,
+                                const void* vt, float* text_part, int n_text, const WorkItem* items, int n_items) {
   TcParams prm;
   prm.q = static_cast<const char*>(q);
   prm.k = static_cast<const char*>(k);
@@ -755,8 +839,14 @@ cudaError_t launch_attention_bf16_tc(const wsa_plan_s& p, const void* q, const v
   prm.o = static_cast<char*>(o);
   prm.row_map = canonical ? p.d_ids : nullptr;
   prm.offsets = p.d_offsets;
-  prm.items = p.d_tc_items;
-  prm.num_units = p.num_tc_items * heads;
+  prm.items = items;
+  prm.num_units = n_items * heads;
+  prm.qt = static_cast<const char*>(qt);
+  prm.kt = static_cast<const char*>(kt);
+  prm.vt = static_cast<const char*>(vt);
+  prm.text_part = text_part;
+  prm.n_text = n_text;
+  prm.inv_windows = 1.0f / static_cast<float>(p.num_windows);
   prm.heads = heads;
   prm.row_stride = static_cast<long long>(heads) * kD * 2;
   prm.c = scale * 1.4426950408889634f;

@@ -83,5 +83,18 @@ cudaError_t launch_attention_fp32(const wsa_plan_s& p, const float* q, const flo
 cudaError_t launch_attention_bf16_tc(const wsa_plan_s& p, const void* q, const void* k,
                                      const void* v, void* o, int heads, bool canonical,
                                      float scale, cudaStream_t s);
+// General form: optional text segment (n_text > 0, text tensors and fp32
+// partial buffer) and an explicit work list.
+cudaError_t launch_attention_tc(const wsa_plan_s& p, const void* q, const void* k, const void* v, void* o,
+                                int heads, bool canonical, float scale, cudaStream_t s, const void* qt,
+                                const void* kt, const void* vt, float* text_part, int n_text,
+                                const WorkItem* items, int n_items);
+// Workspace of the text form: its work list, then W x n_text x heads x 128
+// fp32 partials.  *items_bytes (optional) receives the work-list part.
+size_t attention_text_workspace_bytes(const wsa_plan_s& p, int n_text, int heads, size_t* items_bytes);
+cudaError_t launch_attention_text_bf16_tc(const wsa_plan_s& p, const void* q, const void* k, const void* v,
+                                          void* o, const void* qt, const void* kt, const void* vt, void* ot,
+                                          int n_text, int heads, bool canonical, float scale,
+                                          void* workspace, cudaStream_t s);
 
 }  // namespace wsa
