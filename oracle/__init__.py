@@ -26,6 +26,7 @@ from .transition import transition, gather_table
 from .attention import (window_attention, masked_full_attention, window_attention_rows,
                         window_attention_text)
 from .planner import lpt_assign
+from . import sp
 
 __all__ = [
     "WINDOW_REF_AREA",
@@ -42,4 +43,5 @@ __all__ = [
     "masked_full_attention",
     "window_attention_text",
     "lpt_assign",
+    "sp",
 ]
