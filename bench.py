@@ -45,8 +45,10 @@ def kernel_sha1():
         return hashlib.sha1(f.read()).hexdigest()[:16]
 
 
-def attn_flops(offsets, heads, d):
-    n = np.diff(np.asarray(offsets, dtype=np.float64))
+def attn_flops(offsets, heads, d, n_text=0):
+    """Algorithmic attention FLOPs of one layer: 4 n^2 d per segment and head,
+    a segment being a window's n_w video tokens plus n_text text tokens."""
+    n = np.diff(np.asarray(offsets, dtype=np.float64)) + n_text
     return float(4.0 * np.sum(n * n) * d * heads)
 
 
@@ -163,11 +165,20 @@ def run_ours(args):
     n_sets = min(L, 4)
     sets = [wsa_inputs.qkv(wl, layer=i, device=dev) for i in range(n_sets)]
     outs = [torch.empty_like(sets[i % n_sets][0]) for i in range(min(L, 2))]
+    n_text = args.text
+    if n_text:
+        # replicated text tokens of each layer's segments (seeded like Q/K/V)
+        tshape = (n_text, wl.heads, wl.head_dim)
+        tsets = [tuple(wsa_inputs.randn(tshape, 900000 + 3 * i + j, dev).to(torch.bfloat16) for j in range(3))
+                 for i in range(n_sets)]
+        touts = [torch.empty(tshape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        wspace = [torch.empty(wsa.attention_text_workspace_bytes(p, n_text, wl.heads), dtype=torch.uint8, device=dev)
+                  for p in plans]
     hidden = [wsa_inputs.activation(wl, device=dev), None]
     hidden[1] = torch.empty_like(hidden[0])
     stream = torch.cuda.current_stream()
 
-    flops = [attn_flops(p.tables()[0].cpu().numpy(), wl.heads, wl.head_dim) for p in plans]
+    flops = [attn_flops(p.tables()[0].cpu().numpy(), wl.heads, wl.head_dim, n_text) for p in plans]
     fl_step = sum(flops[l % 2] for l in range(L))
     trans_bytes = 2.0 * N * C * 2 + 2 * 4.0 * N  # read + write rows, two int32 table reads
 
@@ -179,7 +190,11 @@ def run_ours(args):
         for l in range(L):
             q, k, v = sets[l % n_sets]
             if e: e[2 * l].record(stream)
-            wsa.attention(plans[l % 2], q, k, v, out=outs[l % 2])
+            if n_text:
+                wsa.attention_text(plans[l % 2], q, k, v, *tsets[l % n_sets], out=outs[l % 2],
+                                   out_txt=touts[l % 2], workspace=wspace[l % 2])
+            else:
+                wsa.attention(plans[l % 2], q, k, v, out=outs[l % 2])
             if e: e[2 * l + 1].record(stream)
             if l + 1 < L:
                 wsa.transition(plans[l % 2], plans[(l + 1) % 2], hidden[l % 2], out=hidden[(l + 1) % 2])
@@ -217,7 +232,7 @@ def run_ours(args):
     # workloads): H2D of this step's Q/K/V of both layers and the hidden rows,
     # the three calls, D2H of the two attention outputs and the transitioned rows.
     e2e = None
-    if L == 2 and not args.no_e2e:
+    if L == 2 and not args.no_e2e and not n_text:
         q0, k0, v0 = sets[0]
         q1, k1, v1 = sets[1]
         x, y = hidden
@@ -294,8 +309,9 @@ def run_ours(args):
         "config": {"workload": f"{wl.name}: T={wl.T},H={wl.H},W={wl.W} ({N} tokens), nt,nh,nw={wl.nt},{wl.nh},{wl.nw} "
                                f"-> wt,wh,ww={plans[0].wt},{plans[0].wh},{plans[0].ww}; {wl.heads} heads x {wl.head_dim}; "
                                f"{L} alternating layers (attention gathers/scatters through ids) with "
-                               f"{L - 1} transitions of [N,{C}]",
-                   "tokens": N, "heads": wl.heads, "head_dim": wl.head_dim, "layers": L,
+                               f"{L - 1} transitions of [N,{C}]"
+                               + (f"; segments [window, {n_text} text tokens], text mean over windows" if n_text else ""),
+                   "tokens": N, "heads": wl.heads, "head_dim": wl.head_dim, "layers": L, "text_tokens": n_text,
                    "windows": [plans[0].num_windows, plans[1].num_windows],
                    "l2": "inputs larger than L2 (Q/K/V >= 155 MB each); no flush",
                    "parallelism": "replicas" if ws > 1 else "single"},
@@ -313,7 +329,7 @@ def run_ours(args):
             "traffic_note": traffic_note,
         },
         "e2e": e2e,
-        "gpu_launches": (2 * L - 1) * args.steps,
+        "gpu_launches": ((3 if n_text else 2) * L - 1) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -403,6 +419,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (small profiling case)")
+    ap.add_argument("--text", type=int, default=0, help="replicated text tokens appended to every window segment")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

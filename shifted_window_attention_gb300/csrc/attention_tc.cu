@@ -335,6 +335,7 @@ __device__ __forceinline__ uint32_t bar_at(const Smem& s, int i) { return s.bars
 // gather warps never wait for data; the MMA thread makes the landed rows
 // visible to the tensor core with a proxy fence.  The token ids of the next
 // key tile are fetched while the current one is issued.
+template <bool kText>
 __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm, int lw, int lane) {
   int* err = prm.work + WS_ERROR;
   const int half = lane >> 4;
@@ -355,26 +356,42 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
       const int myrow = row0 + kLoaderRows * lw + 32 * h + lane;
       ids[h] = -1;
       if (myrow < nv) ids[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
-      else if (myrow < n) ids[h] = -2 - (myrow - nv);
+      else if (kText && myrow < n) ids[h] = -2 - (myrow - nv);
     }
   };
-  auto copy_tile = [&](const char* src, const char* tsrc, uint32_t dst, const int (&ids)[2], int head) {
+  // A tile that reaches the text rows (warp-uniform `text`, text kernel only)
+  // selects between two sources per row in a rolled loop; every other tile
+  // keeps the unrolled single-source address path.  Both the extra select and
+  // a second unrolled copy of the loop slow the gather warps, whose issue rate
+  // bounds the kernel.
+  auto copy_tile = [&](const char* src, const char* tsrc, uint32_t dst, const int (&ids)[2], int head, bool text) {
     const long long col = static_cast<long long>(head) * (kD * 2) + chunk * 16;
+    if (!kText || !text) {
+      const char* colbase = src + col;
 #pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int r = kLoaderRows * lw + half + 2 * i;
+        const int id = __shfl_sync(0xffffffffu, ids[i >> 4], half + 2 * (i & 15));
+        const char* g = id >= 0 ? colbase + static_cast<long long>(id) * prm.row_stride : src;
+        cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
+      }
+      return;
+    }
+#pragma unroll 1
     for (int i = 0; i < 32; ++i) {
       const int r = kLoaderRows * lw + half + 2 * i;
-      const int id = __shfl_sync(0xffffffffu, ids[i >> 4], half + 2 * (i & 15));
+      const int id = __shfl_sync(0xffffffffu, i < 16 ? ids[0] : ids[1], half + 2 * (i & 15));
       const char* g = id >= 0 ? src + col + static_cast<long long>(id) * prm.row_stride
                               : (id <= -2 ? tsrc + col + static_cast<long long>(-2 - id) * prm.row_stride : src);
       cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id != -1 ? 16u : 0u);
     }
   };
-  auto load_kv = [&](const int (&ids)[2], int head) -> bool {
+  auto load_kv = [&](const int (&ids)[2], int head, bool text) -> bool {
     for (int which = 0; which < 2; ++which) {
       const uint32_t slot = ring_iter % kSlots;
       if (!acquire(bar_at(sm, B_RING_EMPTY + slot), ((ring_iter / kSlots) & 1) ^ 1, E_LOAD_RING_EMPTY))
         return false;
-      copy_tile(which ? prm.v : prm.k, which ? prm.vt : prm.kt, sm.ring + slot * kTileBytes, ids, head);
+      copy_tile(which ? prm.v : prm.k, which ? prm.vt : prm.kt, sm.ring + slot * kTileBytes, ids, head, text);
       cp_async_arrive(bar_at(sm, B_RING_FULL + slot));
       ++ring_iter;
     }
@@ -387,7 +404,7 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     if (!acquire(bar_at(sm, B_UNIT_FULL + us), uph, E_LOAD_UNIT_FULL)) break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int off = info.x, nv = info.y, n = nv + prm.n_text, q0 = info.z, head = info.w & 0xffff;
+    const int off = info.x, nv = info.y, n = nv + (kText ? prm.n_text : 0), q0 = info.z, head = info.w & 0xffff;
     const int nkv = (n + kTile - 1) / kTile;
     const bool has1 = q0 + kTile < n;
     int ids[2], ids_next[2], qids0[2], qids1[2];
@@ -397,17 +414,17 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     // K0/V0 first: they may land while the previous unit's last MMAs still
     // hold the Q buffers.
     if (nkv > 1) fetch_ids(ids_next, kTile, nv, n, off);
-    if (!load_kv(ids, head)) break;
+    if (!load_kv(ids, head, nv < kTile && n > nv)) break;
     if (!acquire(bar_at(sm, B_Q_EMPTY), (unit_iter & 1) ^ 1, E_LOAD_Q_EMPTY)) break;
-    copy_tile(prm.q, prm.qt, sm.q0, qids0, head);
-    if (has1) copy_tile(prm.q, prm.qt, sm.q0 + kTileBytes, qids1, head);
+    copy_tile(prm.q, prm.qt, sm.q0, qids0, head, q0 + kTile > nv && n > nv);
+    if (has1) copy_tile(prm.q, prm.qt, sm.q0 + kTileBytes, qids1, head, q0 + 2 * kTile > nv && n > nv);
     cp_async_arrive(bar_at(sm, B_Q_FULL));
     bool ok = true;
     for (int j = 1; j < nkv && ok; ++j) {
       ids[0] = ids_next[0];
       ids[1] = ids_next[1];
       if (j + 1 < nkv) fetch_ids(ids_next, (j + 1) * kTile, nv, n, off);
-      ok = load_kv(ids, head);
+      ok = load_kv(ids, head, (j + 1) * kTile > nv && n > nv);
     }
     if (!ok) break;
     __syncwarp();
@@ -443,6 +460,7 @@ __device__ __forceinline__ void scheduler_role(const TcParams& prm, const Smem& 
 // so the softmax of one Q tile overlaps the MMAs of the other.  S_t of tile
 // j+1 overwrites P_t of tile j only after PV_t(j) was issued (tcgen05.mma
 // from one thread execute in order).
+template <bool kText>
 __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, uint32_t tmem) {
   int* err = prm.work + WS_ERROR;
   const uint32_t tS0 = tmem + kColS0, tS1 = tmem + kColS1, tO0 = tmem + kColO0, tO1 = tmem + kColO1;
@@ -453,7 +471,7 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
     if (!wait_bar(bar_at(sm, B_UNIT_FULL + us), (unit_iter >> 1) & 1, err, E_MMA_UNIT_FULL)) break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int n = info.y + prm.n_text, q0 = info.z;
+    const int n = info.y + (kText ? prm.n_text : 0), q0 = info.z;
     const bool has1 = q0 + kTile < n;
     const int nkv = (n + kTile - 1) / kTile;
     bool ok = true;
@@ -611,6 +629,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool firs
 
 // Softmax warps: warp w handles Q tile w/4, TMEM lanes 32*(w%4) .. +31; the
 // thread owns one query row.
+template <bool kText>
 __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm, uint32_t tmem, int warp,
                                              int lane) {
   int* err = prm.work + WS_ERROR;
@@ -627,7 +646,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
       break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int off = info.x, nv = info.y, n = nv + prm.n_text, q0 = info.z, head = info.w & 0xffff;
+    const int off = info.x, nv = info.y, n = nv + (kText ? prm.n_text : 0), q0 = info.z, head = info.w & 0xffff;
     if (t == 0 || q0 + kTile < n) {
       const int nkv = (n + kTile - 1) / kTile;
       float m = -INFINITY;
@@ -654,7 +673,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
       const float inv = 1.f / ((la.x + la.y) + (lb.x + lb.y));
       const int qr = q0 + kTile * t + rq;
       const bool valid = qr < nv;           // a video row of this window
-      const bool text = qr >= nv && qr < n;  // a text row: partial T_w / W
+      const bool text = kText && qr >= nv && qr < n;  // a text row: partial T_w / W
       long long tok = 0;
       if (valid) tok = prm.row_map ? __ldg(prm.row_map + off + qr) : off + qr;
       float* tdst = nullptr;
@@ -668,7 +687,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
         float x[64];
         __syncwarp();
         tmem_ld64(tO + 64 * h, x);
-        if (text) {
+        if (kText && text) {
           const float sc = inv * prm.inv_windows;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
@@ -703,6 +722,7 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
 
 // Registers: each SM sub-partition holds 16K registers and 3 of the 12
 // warps, so 168 registers per thread fit (3 x 32 x 168 = 16,128).
+template <bool kText>
 __global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -743,11 +763,11 @@ __global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp < kLoaderWarp0) {
-    softmax_role(prm, sm, tmem, warp, lane);
+    softmax_role<kText>(prm, sm, tmem, warp, lane);
   } else if (warp < kMmaWarp) {
-    loader_role(prm, sm, warp - kLoaderWarp0, lane);
+    loader_role<kText>(prm, sm, warp - kLoaderWarp0, lane);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_role(prm, sm, tmem);
+    if (lane == 0) mma_role<kText>(prm, sm, tmem);
   } else if (lane == 0) {
     scheduler_role(prm, sm);
   }
@@ -852,10 +872,13 @@ cudaError_t launch_attention_tc(const wsa_plan_s& p, const void* q, const void* 
   prm.c = scale * 1.4426950408889634f;
   prm.o_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 && (prm.row_stride & 31) == 0;
   prm.work = p.d_work;
-  cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  // The text segment is a separate instantiation: its extra row source costs
+  // the video-only kernel's gather warps issue slots even where it never runs.
+  auto kernel = n_text > 0 ? attention_tc_kernel<true> : attention_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(sm_count(), prm.num_units));
-  attention_tc_kernel<<<grid, kThreads, kSmemAlloc, s>>>(prm);
+  kernel<<<grid, kThreads, kSmemAlloc, s>>>(prm);
   return cudaGetLastError();
 }
 
