@@ -108,7 +108,9 @@ struct TcParams {
   int heads;
   // Text segment (n_text = 0: video only).  Window w's attention runs over the
   // segment [its n_w video rows, the n_text text rows]; text query rows write
-  // fp32 partials T_w / W to text_part[w][t][head][128].
+  // fp32 partials T_w / W to text_part[w][t][head][128].  The segment is tiled
+  // as the video rows' ceil(n_w/128) tiles followed by the text rows'
+  // ceil(n_text/128) tiles, so that every tile has a single row source.
   const char* qt;
   const char* kt;
   const char* vt;
@@ -347,51 +349,40 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
   auto acquire = [&](uint32_t bar, uint32_t parity, int code) -> bool {
     return __all_sync(0xffffffffu, wait_bar(bar, parity, err, code));
   };
-  // lane l holds the row sources of segment rows kLoaderRows*lw + l and
-  // + 32 + l of a tile starting at segment row row0: id >= 0 is a video row,
-  // id <= -2 is text row -2 - id, -1 is past the segment end (zero fill).
-  auto fetch_ids = [&](int (&ids)[2], int row0, int nv, int n, int off) {
+  // lane l holds the source rows of rows kLoaderRows*lw + l and + 32 + l of
+  // segment tile j (-1: past the end of its part, zero fill): a video row id
+  // for the first nvt tiles, a text row index for the text tiles after them.
+  auto fetch_ids = [&](int (&ids)[2], int j, int nv, int nvt, int off) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int myrow = row0 + kLoaderRows * lw + 32 * h + lane;
+      const int lr = kLoaderRows * lw + 32 * h + lane;
       ids[h] = -1;
-      if (myrow < nv) ids[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
-      else if (kText && myrow < n) ids[h] = -2 - (myrow - nv);
+      if (!kText || j < nvt) {
+        const int myrow = j * kTile + lr;
+        if (myrow < nv) ids[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+      } else {
+        const int tr = (j - nvt) * kTile + lr;
+        if (tr < prm.n_text) ids[h] = tr;
+      }
     }
   };
-  // A tile that reaches the text rows (warp-uniform `text`, text kernel only)
-  // selects between two sources per row in a rolled loop; every other tile
-  // keeps the unrolled single-source address path.  Both the extra select and
-  // a second unrolled copy of the loop slow the gather warps, whose issue rate
-  // bounds the kernel.
-  auto copy_tile = [&](const char* src, const char* tsrc, uint32_t dst, const int (&ids)[2], int head, bool text) {
-    const long long col = static_cast<long long>(head) * (kD * 2) + chunk * 16;
-    if (!kText || !text) {
-      const char* colbase = src + col;
+  auto copy_tile = [&](const char* src, uint32_t dst, const int (&ids)[2], int head) {
+    const char* colbase = src + static_cast<long long>(head) * (kD * 2) + chunk * 16;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = kLoaderRows * lw + half + 2 * i;
-        const int id = __shfl_sync(0xffffffffu, ids[i >> 4], half + 2 * (i & 15));
-        const char* g = id >= 0 ? colbase + static_cast<long long>(id) * prm.row_stride : src;
-        cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
-      }
-      return;
-    }
-#pragma unroll 1
     for (int i = 0; i < 32; ++i) {
       const int r = kLoaderRows * lw + half + 2 * i;
-      const int id = __shfl_sync(0xffffffffu, i < 16 ? ids[0] : ids[1], half + 2 * (i & 15));
-      const char* g = id >= 0 ? src + col + static_cast<long long>(id) * prm.row_stride
-                              : (id <= -2 ? tsrc + col + static_cast<long long>(-2 - id) * prm.row_stride : src);
-      cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id != -1 ? 16u : 0u);
+      const int id = __shfl_sync(0xffffffffu, ids[i >> 4], half + 2 * (i & 15));
+      const char* g = id >= 0 ? colbase + static_cast<long long>(id) * prm.row_stride : src;
+      cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
     }
   };
-  auto load_kv = [&](const int (&ids)[2], int head, bool text) -> bool {
+  auto load_kv = [&](const int (&ids)[2], int head, bool text) -> bool {  // text: a text tile
     for (int which = 0; which < 2; ++which) {
       const uint32_t slot = ring_iter % kSlots;
       if (!acquire(bar_at(sm, B_RING_EMPTY + slot), ((ring_iter / kSlots) & 1) ^ 1, E_LOAD_RING_EMPTY))
         return false;
-      copy_tile(which ? prm.v : prm.k, which ? prm.vt : prm.kt, sm.ring + slot * kTileBytes, ids, head, text);
+      copy_tile(kText && text ? (which ? prm.vt : prm.kt) : (which ? prm.v : prm.k), sm.ring + slot * kTileBytes, ids,
+                head);
       cp_async_arrive(bar_at(sm, B_RING_FULL + slot));
       ++ring_iter;
     }
@@ -404,27 +395,29 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     if (!acquire(bar_at(sm, B_UNIT_FULL + us), uph, E_LOAD_UNIT_FULL)) break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int off = info.x, nv = info.y, n = nv + (kText ? prm.n_text : 0), q0 = info.z, head = info.w & 0xffff;
-    const int nkv = (n + kTile - 1) / kTile;
-    const bool has1 = q0 + kTile < n;
+    const int off = info.x, nv = info.y, q0 = info.z, head = info.w & 0xffff;
+    const int nvt = (nv + kTile - 1) / kTile;
+    const int nkv = nvt + (kText ? (prm.n_text + kTile - 1) / kTile : 0);
+    const int qt0 = q0 / kTile;
+    const bool has1 = qt0 + 1 < nkv;
     int ids[2], ids_next[2], qids0[2], qids1[2];
-    fetch_ids(ids, 0, nv, n, off);
-    fetch_ids(qids0, q0, nv, n, off);
-    if (has1) fetch_ids(qids1, q0 + kTile, nv, n, off);
+    fetch_ids(ids, 0, nv, nvt, off);
+    fetch_ids(qids0, qt0, nv, nvt, off);
+    if (has1) fetch_ids(qids1, qt0 + 1, nv, nvt, off);
     // K0/V0 first: they may land while the previous unit's last MMAs still
     // hold the Q buffers.
-    if (nkv > 1) fetch_ids(ids_next, kTile, nv, n, off);
-    if (!load_kv(ids, head, nv < kTile && n > nv)) break;
+    if (nkv > 1) fetch_ids(ids_next, 1, nv, nvt, off);
+    if (!load_kv(ids, head, nvt == 0)) break;
     if (!acquire(bar_at(sm, B_Q_EMPTY), (unit_iter & 1) ^ 1, E_LOAD_Q_EMPTY)) break;
-    copy_tile(prm.q, prm.qt, sm.q0, qids0, head, q0 + kTile > nv && n > nv);
-    if (has1) copy_tile(prm.q, prm.qt, sm.q0 + kTileBytes, qids1, head, q0 + 2 * kTile > nv && n > nv);
+    copy_tile(kText && qt0 >= nvt ? prm.qt : prm.q, sm.q0, qids0, head);
+    if (has1) copy_tile(kText && qt0 + 1 >= nvt ? prm.qt : prm.q, sm.q0 + kTileBytes, qids1, head);
     cp_async_arrive(bar_at(sm, B_Q_FULL));
     bool ok = true;
     for (int j = 1; j < nkv && ok; ++j) {
       ids[0] = ids_next[0];
       ids[1] = ids_next[1];
-      if (j + 1 < nkv) fetch_ids(ids_next, (j + 1) * kTile, nv, n, off);
-      ok = load_kv(ids, head, (j + 1) * kTile > nv && n > nv);
+      if (j + 1 < nkv) fetch_ids(ids_next, j + 1, nv, nvt, off);
+      ok = load_kv(ids, head, j >= nvt);
     }
     if (!ok) break;
     __syncwarp();
@@ -471,9 +464,9 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
     if (!wait_bar(bar_at(sm, B_UNIT_FULL + us), (unit_iter >> 1) & 1, err, E_MMA_UNIT_FULL)) break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int n = info.y + (kText ? prm.n_text : 0), q0 = info.z;
-    const bool has1 = q0 + kTile < n;
-    const int nkv = (n + kTile - 1) / kTile;
+    const int q0 = info.z;
+    const int nkv = (info.y + kTile - 1) / kTile + (kText ? (prm.n_text + kTile - 1) / kTile : 0);
+    const bool has1 = q0 / kTile + 1 < nkv;
     bool ok = true;
     uint32_t v_prev = 0, vslot_prev = 0;
     for (int j = 0; j < nkv; ++j) {
@@ -646,9 +639,11 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
       break;
     const int4 info = sm.units[us];
     if (info.y < 0) break;
-    const int off = info.x, nv = info.y, n = nv + (kText ? prm.n_text : 0), q0 = info.z, head = info.w & 0xffff;
-    if (t == 0 || q0 + kTile < n) {
-      const int nkv = (n + kTile - 1) / kTile;
+    const int off = info.x, nv = info.y, q0 = info.z, head = info.w & 0xffff;
+    const int nvt = (nv + kTile - 1) / kTile;
+    const int nkv = nvt + (kText ? (prm.n_text + kTile - 1) / kTile : 0);
+    const int qtile = q0 / kTile + t;
+    if (qtile < nkv) {
       float m = -INFINITY;
       float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
       bool ok = true;
@@ -657,7 +652,8 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
         ++s_iter;
         if (!ok) break;
         tc_fence_after();
-        const int kv_valid = min(kTile, n - j * kTile);
+        const int kv_valid =
+            !kText || j < nvt ? min(kTile, nv - j * kTile) : min(kTile, prm.n_text - (j - nvt) * kTile);
         if (kv_valid == kTile)
           softmax_tile<true>(tS, tO, j == 0, kv_valid, c, m, la, lb);
         else
@@ -671,15 +667,16 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
       ++o_iter;
       tc_fence_after();
       const float inv = 1.f / ((la.x + la.y) + (lb.x + lb.y));
-      const int qr = q0 + kTile * t + rq;
-      const bool valid = qr < nv;           // a video row of this window
-      const bool text = kText && qr >= nv && qr < n;  // a text row: partial T_w / W
+      const bool vtile = !kText || qtile < nvt;
+      const int qr = (vtile ? qtile : qtile - nvt) * kTile + rq;  // row of the video or the text part
+      const bool valid = vtile && qr < nv;                          // a video row of this window
+      const bool text = kText && !vtile && qr < prm.n_text;         // a text row: partial T_w / W
       long long tok = 0;
       if (valid) tok = prm.row_map ? __ldg(prm.row_map + off + qr) : off + qr;
       float* tdst = nullptr;
       if (text) {
         const long long window = static_cast<unsigned>(info.w) >> 16;
-        tdst = prm.text_part + ((window * prm.n_text + (qr - nv)) * prm.heads + head) * kD;
+        tdst = prm.text_part + ((window * prm.n_text + qr) * prm.heads + head) * kD;
       }
       uint4* dst = reinterpret_cast<uint4*>(prm.o + tok * prm.row_stride + static_cast<long long>(head) * (kD * 2));
 #pragma unroll
@@ -810,9 +807,18 @@ __global__ void text_reduce_kernel(const float* __restrict__ part, __nv_bfloat16
 
 }  // namespace
 
+namespace {
+
+// Rows of a text segment as the kernel tiles it: the video part and the text
+// part each padded to whole 128-row tiles.
+int text_segment_rows(int nv, int n_text) { return ((nv + 127) / 128 + (n_text + 127) / 128) * 128; }
+
+}  // namespace
+
 size_t attention_text_workspace_bytes(const wsa_plan_s& p, int n_text, int heads, size_t* items_bytes) {
   std::vector<int> seg(p.h_offsets.size(), 0);
-  for (size_t w = 1; w < seg.size(); ++w) seg[w] = seg[w - 1] + (p.h_offsets[w] - p.h_offsets[w - 1]) + n_text;
+  for (size_t w = 1; w < seg.size(); ++w)
+    seg[w] = seg[w - 1] + text_segment_rows(p.h_offsets[w] - p.h_offsets[w - 1], n_text);
   const size_t n_items = make_items(seg, kTcItemRows, 128).size();
   const size_t ib = (n_items * sizeof(WorkItem) + 255) / 256 * 256;
   if (items_bytes) *items_bytes = ib;
@@ -823,7 +829,8 @@ cudaError_t launch_attention_text_bf16_tc(const wsa_plan_s& p, const void* q, co
                                           const void* qt, const void* kt, const void* vt, void* ot, int n_text,
                                           int heads, bool canonical, float scale, void* workspace, cudaStream_t s) {
   std::vector<int> seg(p.h_offsets.size(), 0);
-  for (size_t w = 1; w < seg.size(); ++w) seg[w] = seg[w - 1] + (p.h_offsets[w] - p.h_offsets[w - 1]) + n_text;
+  for (size_t w = 1; w < seg.size(); ++w)
+    seg[w] = seg[w - 1] + text_segment_rows(p.h_offsets[w] - p.h_offsets[w - 1], n_text);
   const std::vector<WorkItem> items = make_items(seg, kTcItemRows, 128);
   size_t items_bytes = 0;
   attention_text_workspace_bytes(p, n_text, heads, &items_bytes);
