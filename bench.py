@@ -35,7 +35,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # 24-head 720p workload: an ncu capture of the same grid with 8 heads measured
 # 884.9 MB, scaled x3 (each head's rows are disjoint, so traffic grows with the
 # head count).  Valid only for the kernel source it was measured on.
-MEASURED_TRAFFIC = {"kernel_sha1": "b5473f6a6dfaaa3f", "workload": "720p", "heads": 24, "bytes": 2.655e9}
+MEASURED_TRAFFIC = {"kernel_sha1": "943d25a92817746c", "workload": "720p", "heads": 24, "bytes": 2.655e9}
 
 
 def kernel_sha1():
@@ -341,6 +341,82 @@ def run_ours(args):
     return result if rank == 0 else None
 
 
+def run_plan_a(args):
+    """Plan A device kernels at a layout boundary, ranks emulated on one GPU.
+
+    Each of R emulated ranks packs its rows (wsa_gather_rows through
+    send_index) and unpacks its receive buffer (through recv_index), for both
+    boundaries regular -> shifted and shifted -> regular.  The collective
+    between them is not timed: on one GPU it is emulated by slicing the send
+    buffers into receive buffers once, before the timed region.  Algorithmic
+    bytes per boundary: every row is read and written once by a pack and once
+    by an unpack, plus one int32 index read per row for each."""
+    import torch
+    import shifted_window_attention_gb300.sp as sp
+    import wsa_inputs
+
+    wl = wsa_inputs.WORKLOADS[args.workload]
+    R = args.plan_a
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    grid = (wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw)
+    N, C = wl.num_tokens, wl.channels
+    x = wsa_inputs.activation(wl, device=dev)
+    legs = []
+    for src_l, dst_l in ((0, 1), (1, 0)):
+        plans = [sp.PlanA(*grid, src_l, dst_l, R, r) for r in range(R)]
+        xl = [x[torch.from_numpy(sp.local_rows(*grid, src_l, R, r).astype(np.int64)).to(dev)].contiguous()
+              for r in range(R)]
+        sends = [torch.empty((p.n_send, C), dtype=x.dtype, device=dev) for p in plans]
+        for r in range(R):
+            plans[r].pack(xl[r], out=sends[r])
+        bounds = [np.concatenate([[0], np.cumsum(p.input_split_sizes)]) for p in plans]
+        recvs = [torch.cat([sends[r][bounds[r][d]:bounds[r][d + 1]] for r in range(R)]).contiguous()
+                 for d in range(R)]
+        outs = [torch.empty((p.n_recv, C), dtype=x.dtype, device=dev) for p in plans]
+        legs.append((plans, xl, sends, recvs, outs))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for plans, xl, sends, recvs, outs in legs:
+            for r in range(R):
+                plans[r].pack(xl[r], out=sends[r])
+            for d in range(R):
+                plans[d].unpack(recvs[d], out=outs[d])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    step_bytes = 2 * (2 * (2.0 * N * C * x.element_size()) + 2 * 4.0 * N)
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    peaks, peak_kind = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    return {
+        "metric": "Plan A pack + unpack bandwidth (both boundaries, ranks emulated on one GPU)",
+        "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded torch.randn rows, bf16)",
+        "config": {"workload": f"{wl.name}: [N={N}, C={C}] hidden rows, {R} emulated ranks, regular <-> shifted; "
+                               "collective emulated outside the timed region",
+                   "ranks": R, "l2": "inputs larger than L2 (464 MB of rows); no flush"},
+        "roofline": {"bound": "hbm", "kernel": "transition_rows_kernel (one-level gather)",
+                     "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs / hbm, 4), "peak_source": f"{peak_kind} copy bandwidth", "traffic": None},
+        "gpu_launches": 4 * R * args.steps,
+        "clocks": clk,
+    }
+
+
 def cpu_inputs(wl):
     """The workload's layer-0 Q/K/V as fp32 numpy arrays (drawn on the GPU when
     one is present, which is faster; the CPU draw otherwise)."""
@@ -420,10 +496,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (small profiling case)")
     ap.add_argument("--text", type=int, default=0, help="replicated text tokens appended to every window segment")
+    ap.add_argument("--plan-a", type=int, default=0,
+                    help="time the Plan A pack/unpack kernels for this many emulated ranks instead")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.plan_a and args.impl == "ours":
+        res = run_plan_a(args)
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 

@@ -211,6 +211,68 @@ wsa_status wsa_attention_noalloc(int T, int H, int W, int nt, int nh, int nw,
                                  float softmax_scale, void* stream);
 
 /*
+ * Window-aligned sequence parallelism, Plan A ("Window-Aligned Sequence
+ * Parallelism (SeedVR2)", sections "Planner" and "Plan A redistribution").
+ * Whole windows are sharded over `ranks` ranks.  The LPT rule takes windows
+ * by (-token count, window id) and gives each to the rank with the smallest
+ * (assigned tokens, rank id).  A rank lists its windows in ascending id and
+ * holds their rows (row-major in (t, h, w) inside a window) in that order;
+ * this is its rank-local order.  The grid arguments are those of
+ * wsa_plan_create.  These three calls run on the host only and need no GPU.
+ * Each writes its counts always and fills an array only when the array is
+ * non-NULL; a capacity smaller than the count is WSA_ERR_INVALID_ARG.
+ *
+ * wsa_sp_owners: owner[w] = rank holding window w of `layout`
+ *   (num_windows entries).  ranks > 0.
+ */
+wsa_status wsa_sp_owners(int T, int H, int W, int nt, int nh, int nw,
+                         wsa_layout layout, int max_temporal, int ranks,
+                         int* owner, int capacity, int* num_windows);
+
+/* wsa_sp_local_rows: ids[i] = canonical id of row i of `rank`'s rank-local
+ * order in `layout` (*n_rows entries).  0 <= rank < ranks. */
+wsa_status wsa_sp_local_rows(int T, int H, int W, int nt, int nh, int nw,
+                             wsa_layout layout, int max_temporal, int ranks,
+                             int rank, int* ids, int capacity, int* n_rows);
+
+/*
+ * wsa_sp_plan_a: the exchange of `rank` at the boundary src_layout ->
+ * dst_layout.
+ *   counts [ranks * ranks] (may be NULL): the global count matrix, with
+ *     counts[s * ranks + d] the rows rank d needs from rank s.  Rank r's
+ *     input split sizes are row r; its output split sizes are column r.
+ *   send_index [*n_send]: send row i holds local source row send_index[i].
+ *     Rows are grouped by destination rank, and within a group they are in
+ *     the destination's rank-local order.
+ *   recv_index [*n_recv]: destination-local row p is receive row
+ *     recv_index[p], the argsort of the received rows' destination
+ *     positions.  The receive buffer is the source ranks' segments
+ *     concatenated in rank order.
+ *   *network_exchange_required: 1 if any row changes rank.  It is computed
+ *     from the global matrix, so every rank gets the same value.  When it is
+ *     0, the exchange is the local permutation x[send_index[recv_index[p]]].
+ * Both index tables are int32 on the host; rows counts fit in int.
+ */
+wsa_status wsa_sp_plan_a(int T, int H, int W, int nt, int nh, int nw,
+                         wsa_layout src_layout, wsa_layout dst_layout,
+                         int max_temporal, int ranks, int rank,
+                         long long* counts, int* send_index, int send_capacity,
+                         int* recv_index, int recv_capacity, int* n_send,
+                         int* n_recv, int* network_exchange_required);
+
+/*
+ * wsa_gather_rows -- y[i] = x[index[i]] for 0 <= i < rows: the pack
+ * (index = send_index) and unpack (index = recv_index) steps of the Plan A
+ * exchange, on the device.
+ * x: device, [x_rows, channels]; y: device, [rows, channels]; both of
+ * `dtype` and contiguous; they must not overlap.  index: device int32 [rows].
+ * An index outside [0, x_rows) leaves its row of y unwritten; it is not
+ * reported.  rows == 0 is a no-op.  Bit-exact (pure data movement).
+ */
+wsa_status wsa_gather_rows(const void* x, int x_rows, const int* index, void* y,
+                           int rows, int channels, wsa_dtype dtype, void* stream);
+
+/*
  * Reads and clears the plan's device error word (synchronises the device).
  * *code = 0 when no kernel recorded an error; otherwise the code of the first
  * bounded wait that gave up, and the call returns WSA_ERR_DEVICE_CHECK.

@@ -59,6 +59,10 @@ def _load():
         "wsa_attention_noalloc": ([i] * 8 + [p, p, p, p, i, i, f, p], i),
         "wsa_attention_text_workspace": ([p, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)], i),
         "wsa_attention_text": ([p] + [p] * 8 + [i, i, i, i, i, f, p, ctypes.c_size_t, p], i),
+        "wsa_sp_owners": ([i] * 9 + [ip, i, ip], i),
+        "wsa_sp_local_rows": ([i] * 10 + [ip, i, ip], i),
+        "wsa_sp_plan_a": ([i] * 11 + [ctypes.POINTER(ctypes.c_longlong), ip, i, ip, i, ip, ip, ip], i),
+        "wsa_gather_rows": ([p, i, p, p, i, i, i, p], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -243,6 +247,24 @@ def transition(src, dst, x, out=None, stream=None):
     return out
 
 
+def gather_rows(x, index, out=None, stream=None):
+    """wsa_gather_rows: out[i] = x[index[i]] (the pack and unpack steps of
+    the Plan A exchange).  x: contiguous 2-D CUDA tensor; index: int32 CUDA
+    tensor.  Indices outside [0, len(x)) leave their rows unwritten."""
+    if not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
+        raise WsaError(-1, "x must be a contiguous 2-D CUDA tensor")
+    if not index.is_cuda or index.dtype != torch.int32 or not index.is_contiguous() or index.dim() != 1:
+        raise WsaError(-1, "index must be a contiguous 1-D int32 CUDA tensor")
+    rows = index.shape[0]
+    if out is None:
+        out = torch.empty((rows, x.shape[1]), dtype=x.dtype, device=x.device)
+    elif out.shape != (rows, x.shape[1]) or out.dtype != x.dtype or not out.is_contiguous():
+        raise WsaError(-1, "out must be [len(index), channels] of x's dtype")
+    _check(lib.wsa_gather_rows(_ptr(x), x.shape[0], _ptr(index), _ptr(out), rows, x.shape[1], _dtype_code(x),
+                               _stream(stream)))
+    return out
+
+
 def attention_noalloc(T, H, W, nt, nh, nw, layout, q, k, v, out, canonical=True, scale=0.0,
                       max_temporal=30, stream=None):
     """wsa_attention_noalloc: bf16 window attention of one layout without a
@@ -262,5 +284,5 @@ def attention_noalloc(T, H, W, nt, nh, nw, layout, q, k, v, out, canonical=True,
 __all__ = [
     "REGULAR", "SHIFTED", "BF16", "FP32", "WsaError", "Plan", "attention", "transition",
     "window_size", "layout_windows", "version", "lib", "attention_noalloc", "attention_text",
-    "attention_text_workspace_bytes",
+    "attention_text_workspace_bytes", "gather_rows",
 ]

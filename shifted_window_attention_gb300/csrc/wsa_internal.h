@@ -77,6 +77,10 @@ namespace wsa {
 cudaError_t launch_plan_tables(const wsa_plan_s& p, cudaStream_t s);
 cudaError_t launch_transition(const wsa_plan_s& src, const wsa_plan_s& dst, const void* x_src,
                               void* x_dst, size_t row_bytes, cudaStream_t s);
+// y[i] = x[index[i]] for i < rows; rows whose index is outside [0, x_rows)
+// are skipped.
+cudaError_t launch_gather_rows(const void* x, int x_rows, const int* index, void* y, int rows, size_t row_bytes,
+                               cudaStream_t s);
 cudaError_t launch_attention_fp32(const wsa_plan_s& p, const float* q, const float* k,
                                   const float* v, float* o, int heads, int head_dim,
                                   bool canonical, float scale, cudaStream_t s);

@@ -1,0 +1,100 @@
+"""The library's Plan A host planner (wsa_sp_owners, wsa_sp_local_rows,
+wsa_sp_plan_a; no GPU) against the oracle ("Window-Aligned Sequence
+Parallelism (SeedVR2)", sections "Planner" and "Plan A redistribution").
+Integer tables: bit-exact."""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import sp as osp
+from wsa_inputs import WORKLOADS
+
+GRIDS = {
+    "tiny": (4, 9, 16, 2, 9, 16),
+    "odd": (7, 5, 11, 3, 2, 4),
+    "720p": (21, 45, 80, 4, 3, 3),
+    "1080p": (21, 68, 120, 4, 3, 3),
+}
+
+
+@pytest.fixture(scope="module")
+def sp():
+    import __graft_entry__
+    __graft_entry__.build()
+    import shifted_window_attention_gb300.sp as m
+    return m
+
+
+@pytest.mark.parametrize("name", list(GRIDS))
+@pytest.mark.parametrize("ranks", [1, 2, 3, 8])
+@pytest.mark.parametrize("layouts", [(0, 1), (1, 0), (1, 1)])
+def test_plan_a_matches_oracle(sp, name, ranks, layouts):
+    grid = GRIDS[name]
+    src, dst = oracle.make_plan(*grid, layouts[0]), oracle.make_plan(*grid, layouts[1])
+    ref = osp.plan_a(src, dst, ranks)
+    assert np.array_equal(sp.owners(*grid, layouts[0], ranks), osp.owners(src, ranks))
+    for r in range(ranks):
+        pa = sp.PlanA(*grid, *layouts, ranks, r)
+        assert np.array_equal(pa.counts, ref["counts"])
+        assert pa.input_split_sizes == list(ref["counts"][r])
+        assert pa.output_split_sizes == list(ref["counts"][:, r])
+        assert np.array_equal(pa.send_index, ref["send_index"][r])
+        assert np.array_equal(pa.recv_index, ref["recv_index"][r])
+        assert pa.network_exchange_required == ref["network_exchange_required"]
+        assert np.array_equal(sp.local_rows(*grid, layouts[0], ranks, r), ref["src_rows"][r])
+
+
+def test_host_exchange_reproduces_destination_rows(sp):
+    # Run the schedule on the host (index arithmetic only): every rank ends
+    # with exactly its destination rows.
+    grid, R = GRIDS["720p"], 4
+    x = np.arange(75600, dtype=np.int64)
+    plans = [sp.PlanA(*grid, 0, 1, R, r) for r in range(R)]
+    local = [x[sp.local_rows(*grid, 0, R, r)] for r in range(R)]
+    sends = [local[r][plans[r].send_index] for r in range(R)]
+    bounds = [np.concatenate([[0], np.cumsum(p.input_split_sizes)]) for p in plans]
+    for d in range(R):
+        recv = np.concatenate([sends[r][bounds[r][d]:bounds[r][d + 1]] for r in range(R)])
+        assert np.array_equal(recv[plans[d].recv_index], sp.local_rows(*grid, 1, R, d))
+
+
+def test_same_layout_is_local(sp):
+    grid = GRIDS["720p"]
+    for r in range(3):
+        pa = sp.PlanA(*grid, 1, 1, 3, r)
+        assert not pa.network_exchange_required
+        assert pa.input_split_sizes[r] == pa.n_send and sum(pa.input_split_sizes) == pa.n_send
+        # the composed fast-path index is the identity: nothing moves
+        assert np.array_equal(pa.send_index[pa.recv_index], np.arange(pa.n_send))
+
+
+def test_more_ranks_than_windows(sp):
+    grid = (2, 3, 4, 1, 1, 1)  # one window in either layout
+    plans = [sp.PlanA(*grid, 0, 1, 3, r) for r in range(3)]
+    assert [p.n_send for p in plans] == [24, 0, 0] and [p.n_recv for p in plans] == [24, 0, 0]
+    assert not plans[1].network_exchange_required
+
+
+def test_errors(sp):
+    import ctypes
+    from shifted_window_attention_gb300 import WsaError
+    with pytest.raises(WsaError, match="INVALID_ARG"):
+        sp.PlanA(*GRIDS["tiny"], 0, 1, 0, 0)
+    with pytest.raises(WsaError, match="INVALID_ARG"):
+        sp.PlanA(*GRIDS["tiny"], 0, 1, 2, 2)
+    with pytest.raises(WsaError, match="INVALID_ARG"):
+        sp.PlanA(*GRIDS["tiny"], 0, 7, 2, 0)
+    with pytest.raises(WsaError, match="INVALID_ARG"):
+        sp.owners(0, 9, 16, 2, 9, 16, 0, 2)
+    lib = sp.lib
+    n_send, n_recv, cross = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    small = (ctypes.c_int * 3)()
+    st = lib.wsa_sp_plan_a(*GRIDS["tiny"], 0, 1, 30, 2, 0, None, small, 3, None, 0, ctypes.byref(n_send),
+                           ctypes.byref(n_recv), ctypes.byref(cross))
+    assert st == -1 and n_send.value > 3
+    n = ctypes.c_int()
+    assert lib.wsa_sp_local_rows(*GRIDS["tiny"], 0, 30, 2, 0, small, 3, ctypes.byref(n)) == -1
+    assert lib.wsa_gather_rows(None, 0, None, None, 0, 8, 0, None) == 0   # rows == 0: no-op
+    assert lib.wsa_gather_rows(None, 4, None, None, 4, 8, 0, None) == -1  # null pointers
+    assert lib.wsa_gather_rows(None, 4, None, None, 4, 0, 0, None) == -1  # channels
