@@ -269,7 +269,8 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     traffic, traffic_note = None, "no ncu capture for this kernel source / workload"
     mt = MEASURED_TRAFFIC
-    if kernel_sha1() == mt["kernel_sha1"] and wl.name == mt["workload"] and wl.heads == mt["heads"]:
+    if (kernel_sha1() == mt["kernel_sha1"] and wl.name == mt["workload"] and wl.heads == mt["heads"]
+            and not n_text):
         traffic = mt["bytes"]
         traffic_note = ("DRAM bytes of the regular-layout launch (ncu capture of the 8-head case scaled x3); "
                         f"algorithmic {4.0 * N * wl.channels * 2:.3e} B")
