@@ -27,6 +27,7 @@ from .attention import (window_attention, masked_full_attention, window_attentio
                         window_attention_text)
 from .planner import lpt_assign
 from . import sp
+from . import rope
 
 __all__ = [
     "WINDOW_REF_AREA",
@@ -44,4 +45,5 @@ __all__ = [
     "window_attention_text",
     "lpt_assign",
     "sp",
+    "rope",
 ]
