@@ -182,22 +182,42 @@ def run_ours(args):
     fl_step = sum(flops[l % 2] for l in range(L))
     trans_bytes = 2.0 * N * C * 2 + 2 * 4.0 * N  # read + write rows, two int32 table reads
 
-    n_ev = 2 * L
+    use_rope = args.rope >= 0
+    if use_rope:
+        # rotated Q/K of the current layer (window-local positions of its layout)
+        qk_rot = [(torch.empty_like(sets[0][0]), torch.empty_like(sets[0][1])) for _ in range(2)]
+        if n_text:
+            tqk_rot = [(torch.empty_like(tsets[0][0]), torch.empty_like(tsets[0][1])) for _ in range(2)]
+    # Q and K rows read + written, the ids table; the text rows when present
+    rope_bytes = 2 * (2.0 * N * C * 2) + 4.0 * N + 2 * (2.0 * n_text * C * 2)
+
+    # per layer: [before RoPE, before attention, after attention, after transition]
+    n_ev = 4 * L
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
 
     def step(i=None):
         e = ev[i] if i is not None else None
         for l in range(L):
             q, k, v = sets[l % n_sets]
-            if e: e[2 * l].record(stream)
+            if e: e[4 * l].record(stream)
+            if use_rope:
+                qr, kr = qk_rot[l % 2]
+                wsa.rope(plans[l % 2], q, k, q_out=qr, k_out=kr, text_len=args.rope)
+                q, k = qr, kr
             if n_text:
-                wsa.attention_text(plans[l % 2], q, k, v, *tsets[l % n_sets], out=outs[l % 2],
+                qt, kt, vt = tsets[l % n_sets]
+                if use_rope:
+                    qt, kt = wsa.rope_text(qt, kt, q_out=tqk_rot[l % 2][0], k_out=tqk_rot[l % 2][1])
+            if e: e[4 * l + 1].record(stream)
+            if n_text:
+                wsa.attention_text(plans[l % 2], q, k, v, qt, kt, vt, out=outs[l % 2],
                                    out_txt=touts[l % 2], workspace=wspace[l % 2])
             else:
                 wsa.attention(plans[l % 2], q, k, v, out=outs[l % 2])
-            if e: e[2 * l + 1].record(stream)
+            if e: e[4 * l + 2].record(stream)
             if l + 1 < L:
                 wsa.transition(plans[l % 2], plans[(l + 1) % 2], hidden[l % 2], out=hidden[(l + 1) % 2])
+            if e: e[4 * l + 3].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -221,8 +241,9 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
-    attn = np.array([[e[2 * l].elapsed_time(e[2 * l + 1]) for l in range(L)] for e in ev])  # [steps, L]
-    trans = np.array([[e[2 * l + 1].elapsed_time(e[2 * l + 2]) for l in range(L - 1)] for e in ev])
+    attn = np.array([[e[4 * l + 1].elapsed_time(e[4 * l + 2]) for l in range(L)] for e in ev])  # [steps, L]
+    trans = np.array([[e[4 * l + 2].elapsed_time(e[4 * l + 3]) for l in range(L - 1)] for e in ev])
+    rope_t = np.array([[e[4 * l].elapsed_time(e[4 * l + 1]) for l in range(L)] for e in ev])
     total_ms = max_over_ranks(total_ms, dist if ws > 1 else None, dev)
     ms_step = total_ms / args.steps
     if any(p.device_status() for p in plans):
@@ -232,7 +253,7 @@ def run_ours(args):
     # workloads): H2D of this step's Q/K/V of both layers and the hidden rows,
     # the three calls, D2H of the two attention outputs and the transitioned rows.
     e2e = None
-    if L == 2 and not args.no_e2e and not n_text:
+    if L == 2 and not args.no_e2e and not n_text and not use_rope:
         q0, k0, v0 = sets[0]
         q1, k1, v1 = sets[1]
         x, y = hidden
@@ -289,6 +310,11 @@ def run_ours(args):
         "transition_frac_hbm": round(trans_bytes / (t_mean * 1e6) / peaks["hbm_gbs"], 4),
         "plan_build_ms_host_incl": round(plan_ms, 3),
     }
+    if use_rope:
+        r_mean = float(rope_t.mean())
+        per_layer["rope_ms"] = round(r_mean, 4)
+        per_layer["rope_gbs"] = round(rope_bytes / (r_mean * 1e6), 1)
+        per_layer["rope_frac_hbm"] = round(rope_bytes / (r_mean * 1e6) / peaks["hbm_gbs"], 4)
     if L > 2:
         per_layer["attention_ms_by_layer"] = [round(float(x), 4) for x in attn.mean(axis=0)]
         per_layer["transition_ms_by_boundary"] = [round(float(x), 4) for x in trans.mean(axis=0)]
@@ -311,7 +337,9 @@ def run_ours(args):
                                f"-> wt,wh,ww={plans[0].wt},{plans[0].wh},{plans[0].ww}; {wl.heads} heads x {wl.head_dim}; "
                                f"{L} alternating layers (attention gathers/scatters through ids) with "
                                f"{L - 1} transitions of [N,{C}]"
-                               + (f"; segments [window, {n_text} text tokens], text mean over windows" if n_text else ""),
+                               + (f"; segments [window, {n_text} text tokens], text mean over windows" if n_text else "")
+                               + (f"; window-local 3D RoPE of Q/K (text_len {args.rope}) before each attention"
+                                  if use_rope else ""),
                    "tokens": N, "heads": wl.heads, "head_dim": wl.head_dim, "layers": L, "text_tokens": n_text,
                    "windows": [plans[0].num_windows, plans[1].num_windows],
                    "l2": "inputs larger than L2 (Q/K/V >= 155 MB each); no flush",
@@ -330,7 +358,8 @@ def run_ours(args):
             "traffic_note": traffic_note,
         },
         "e2e": e2e,
-        "gpu_launches": ((3 if n_text else 2) * L - 1) * args.steps,
+        "gpu_launches": (((2 if n_text else 1) + (0 if not use_rope else 2 if n_text else 1)) * L + L - 1)
+                        * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -497,6 +526,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (small profiling case)")
     ap.add_argument("--text", type=int, default=0, help="replicated text tokens appended to every window segment")
+    ap.add_argument("--rope", type=int, default=-1,
+                    help="apply window-local 3D RoPE to Q/K before every attention, with this text_len (>= 0)")
     ap.add_argument("--plan-a", type=int, default=0,
                     help="time the Plan A pack/unpack kernels for this many emulated ranks instead")
     args = ap.parse_args()

@@ -211,6 +211,47 @@ wsa_status wsa_attention_noalloc(int T, int H, int W, int nt, int nh, int nw,
                                  float softmax_scale, void* stream);
 
 /*
+ * wsa_rope -- window-local 3D rotary position embedding of Q and K.
+ * "Window-Aligned Sequence Parallelism (SeedVR2)", section "Reference quirks
+ * reproduced on purpose": RoPE positions are window-local.  A video token at
+ * (dt, dh, dw) inside its window of `plan` takes the axial indices
+ * (text_len + dt, dh, dw), and every window restarts at 0.  Only the first
+ * 3 * (rope_dim // 3) channels of each head rotate (126 of 128 when
+ * rope_dim = 128); the rest pass through.
+ * Readings of what the note leaves open:
+ *   - axis a of (t, h, w) owns channels [a*da, (a+1)*da), da = rope_dim / 3;
+ *   - channels (2j, 2j+1) of an axis are rotation pair j, turned by
+ *     pos_a * theta^(-2j/da): (x0, x1) -> (x0 c - x1 s, x0 s + x1 c);
+ *   - theta <= 0 selects 10000.
+ * q, k (inputs) and q_out, k_out (outputs): device, [N, heads, head_dim]
+ *   contiguous of `dtype`, rows canonical (in_order_canonical = 1) or
+ *   plan-packed (0), as in wsa_attention; 16-byte aligned.  k and k_out may
+ *   both be NULL (rotate q only).  An output may be its own input (in place)
+ *   but must not overlap anything else.
+ * head_dim 64 or 128; 0 < rope_dim <= head_dim with rope_dim / 3 even
+ *   (WSA_ERR_UNSUPPORTED otherwise); 0 <= text_len <= 2^20.
+ * The rotation is computed in fp32 and rounded once to `dtype`.  The layout
+ * fixes the positions, so Q and K are rotated for the layout the next
+ * attention call uses.
+ */
+wsa_status wsa_rope(wsa_plan_t plan, const void* q, const void* k, void* q_out,
+                    void* k_out, int heads, int head_dim, wsa_dtype dtype,
+                    int in_order_canonical, int text_len, int rope_dim,
+                    float theta, void* stream);
+
+/*
+ * wsa_rope_text -- the same rotation for the replicated text rows
+ * [n_text, heads, head_dim].  Text token i takes the axial indices (i, i, i):
+ * text occupies indices [0, text_len) of the first axis, which is why the
+ * video's first index starts at text_len (reading of the same section).
+ * Other arguments as in wsa_rope; n_text = 0 is a no-op.
+ */
+wsa_status wsa_rope_text(const void* q_txt, const void* k_txt, void* q_out,
+                         void* k_out, int n_text, int heads, int head_dim,
+                         wsa_dtype dtype, int rope_dim, float theta,
+                         void* stream);
+
+/*
  * Window-aligned sequence parallelism, Plan A ("Window-Aligned Sequence
  * Parallelism (SeedVR2)", sections "Planner" and "Plan A redistribution").
  * Whole windows are sharded over `ranks` ranks.  The LPT rule takes windows

@@ -63,6 +63,8 @@ def _load():
         "wsa_sp_local_rows": ([i] * 10 + [ip, i, ip], i),
         "wsa_sp_plan_a": ([i] * 11 + [ctypes.POINTER(ctypes.c_longlong), ip, i, ip, i, ip, ip, ip], i),
         "wsa_gather_rows": ([p, i, p, p, i, i, i, p], i),
+        "wsa_rope": ([p, p, p, p, p, i, i, i, i, i, i, f, p], i),
+        "wsa_rope_text": ([p, p, p, p, i, i, i, i, i, f, p], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -247,6 +249,43 @@ def transition(src, dst, x, out=None, stream=None):
     return out
 
 
+def _rope_args(q, k, q_out, k_out):
+    for t in (q, k):
+        if t is not None and (not t.is_cuda or not t.is_contiguous() or t.dim() != 3):
+            raise WsaError(-1, "q and k must be contiguous 3-D CUDA tensors")
+    if k is not None and (k.shape != q.shape or k.dtype != q.dtype):
+        raise WsaError(-1, "q and k must share shape and dtype")
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    if k is not None:
+        k_out = torch.empty_like(k) if k_out is None else k_out
+    for o in (q_out, k_out):
+        if o is not None and (o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous()):
+            raise WsaError(-1, "outputs must match q")
+    return q_out, k_out
+
+
+def rope(plan, q, k=None, q_out=None, k_out=None, canonical=True, text_len=0, rope_dim=None, theta=10000.0,
+         stream=None):
+    """wsa_rope: window-local 3D RoPE of q (and k) for ``plan``'s windows.
+    Pass q_out=q (k_out=k) to rotate in place.  Returns (q_out, k_out)."""
+    q_out, k_out = _rope_args(q, k, q_out, k_out)
+    rd = q.shape[2] if rope_dim is None else rope_dim
+    _check(lib.wsa_rope(plan.handle, _ptr(q), _ptr(k) if k is not None else None, _ptr(q_out),
+                        _ptr(k_out) if k_out is not None else None, q.shape[1], q.shape[2], _dtype_code(q),
+                        1 if canonical else 0, int(text_len), rd, float(theta), _stream(stream)))
+    return q_out, k_out
+
+
+def rope_text(q_txt, k_txt=None, q_out=None, k_out=None, rope_dim=None, theta=10000.0, stream=None):
+    """wsa_rope_text: RoPE of the text rows, token i at (i, i, i)."""
+    q_out, k_out = _rope_args(q_txt, k_txt, q_out, k_out)
+    rd = q_txt.shape[2] if rope_dim is None else rope_dim
+    _check(lib.wsa_rope_text(_ptr(q_txt), _ptr(k_txt) if k_txt is not None else None, _ptr(q_out),
+                             _ptr(k_out) if k_out is not None else None, q_txt.shape[0], q_txt.shape[1],
+                             q_txt.shape[2], _dtype_code(q_txt), rd, float(theta), _stream(stream)))
+    return q_out, k_out
+
+
 def gather_rows(x, index, out=None, stream=None):
     """wsa_gather_rows: out[i] = x[index[i]] (the pack and unpack steps of
     the Plan A exchange).  x: contiguous 2-D CUDA tensor; index: int32 CUDA
@@ -284,5 +323,5 @@ def attention_noalloc(T, H, W, nt, nh, nw, layout, q, k, v, out, canonical=True,
 __all__ = [
     "REGULAR", "SHIFTED", "BF16", "FP32", "WsaError", "Plan", "attention", "transition",
     "window_size", "layout_windows", "version", "lib", "attention_noalloc", "attention_text",
-    "attention_text_workspace_bytes", "gather_rows",
+    "attention_text_workspace_bytes", "gather_rows", "rope", "rope_text",
 ]

@@ -14,7 +14,7 @@ BUILD_DIR = os.path.join(REPO_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libwsa.so")
 
 SOURCES = ["plan.cu", "transition.cu", "attention_fp32.cu", "attention_tc.cu", "abi.cu",
-           "attention_noalloc.cu", "sp.cu"]
+           "attention_noalloc.cu", "sp.cu", "rope.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -124,6 +124,75 @@ wsa_status wsa_attention_text(wsa_plan_t plan, const void* q, const void* k, con
   return WSA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Shared checks of wsa_rope and wsa_rope_text.  Outputs may alias their own
+// input exactly (in place) but must not overlap anything else.
+wsa_status check_rope(const void* q, const void* k, void* q_out, void* k_out, long long rows, int heads,
+                      int head_dim, wsa_dtype dtype, int rope_dim, float theta, size_t* bytes) {
+  if (!q || !q_out) return fail(WSA_ERR_INVALID_ARG, "q and q_out must be non-null");
+  if ((k == nullptr) != (k_out == nullptr))
+    return fail(WSA_ERR_INVALID_ARG, "k and k_out must both be set or both null");
+  if (heads <= 0) return fail(WSA_ERR_INVALID_ARG, "heads must be > 0");
+  if (dtype != WSA_BF16 && dtype != WSA_FP32) return fail(WSA_ERR_INVALID_ARG, "unknown dtype");
+  if (head_dim != 64 && head_dim != 128) return fail(WSA_ERR_UNSUPPORTED, "rope supports head_dim 64 or 128");
+  if (rope_dim <= 0 || rope_dim > head_dim) return fail(WSA_ERR_INVALID_ARG, "rope_dim must be in [1, head_dim]");
+  if ((rope_dim / 3) % 2 != 0 || rope_dim / 3 < 2)
+    return fail(WSA_ERR_UNSUPPORTED, "rope_dim / 3 (channels per axis) must be even and >= 2");
+  if (!std::isfinite(theta)) return fail(WSA_ERR_INVALID_ARG, "theta is not finite");
+  if (!aligned16(q) || !aligned16(q_out) || (k && (!aligned16(k) || !aligned16(k_out))))
+    return fail(WSA_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  const size_t b = static_cast<size_t>(rows) * heads * head_dim * (dtype == WSA_BF16 ? 2 : 4);
+  auto bad = [&](const void* out, const void* in) { return out != in && overlap(out, b, in, b); };
+  if (bad(q_out, q) || (k && (bad(q_out, k) || bad(k_out, k) || bad(k_out, q) || overlap(q_out, b, k_out, b))))
+    return fail(WSA_ERR_INVALID_ARG, "an output overlaps another tensor (only exact in-place is allowed)");
+  *bytes = b;
+  return WSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+wsa_status wsa_rope(wsa_plan_t plan, const void* q, const void* k, void* q_out, void* k_out, int heads,
+                    int head_dim, wsa_dtype dtype, int in_order_canonical, int text_len, int rope_dim, float theta,
+                    void* stream) {
+  if (!plan) return fail(WSA_ERR_INVALID_ARG, "plan is null");
+  if (in_order_canonical != 0 && in_order_canonical != 1)
+    return fail(WSA_ERR_INVALID_ARG, "in_order_canonical must be 0 or 1");
+  if (text_len < 0 || text_len > (1 << 20)) return fail(WSA_ERR_INVALID_ARG, "text_len must be in [0, 2^20]");
+  size_t bytes = 0;
+  wsa_status st = check_rope(q, k, q_out, k_out, plan->num_tokens, heads, head_dim, dtype, rope_dim, theta, &bytes);
+  if (st != WSA_OK) return st;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_rope: cudaGetDevice");
+  if (dev != plan->device) return fail(WSA_ERR_INVALID_ARG, "plan was created on another device");
+  const void* x[2] = {q, k};
+  void* y[2] = {q_out, k_out};
+  e = launch_rope(plan, in_order_canonical == 1, x, y, k ? 2 : 1, plan->num_tokens, heads, head_dim,
+                  dtype == WSA_BF16, text_len, rope_dim, theta > 0.f ? theta : 10000.0,
+                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_rope: launch");
+  return WSA_OK;
+}
+
+wsa_status wsa_rope_text(const void* q_txt, const void* k_txt, void* q_out, void* k_out, int n_text, int heads,
+                         int head_dim, wsa_dtype dtype, int rope_dim, float theta, void* stream) {
+  if (n_text < 0 || n_text > (1 << 20)) return fail(WSA_ERR_INVALID_ARG, "n_text must be in [0, 2^20]");
+  size_t bytes = 0;
+  wsa_status st = check_rope(q_txt, k_txt, q_out, k_out, n_text, heads, head_dim, dtype, rope_dim, theta, &bytes);
+  if (st != WSA_OK) return st;
+  const void* x[2] = {q_txt, k_txt};
+  void* y[2] = {q_out, k_out};
+  cudaError_t e = launch_rope(nullptr, false, x, y, k_txt ? 2 : 1, n_text, heads, head_dim, dtype == WSA_BF16, 0,
+                              rope_dim, theta > 0.f ? theta : 10000.0, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_rope_text: launch");
+  return WSA_OK;
+}
+
 wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src, void* x_dst, int channels,
                           wsa_dtype dtype, void* stream) {
   if (!src || !dst) return fail(WSA_ERR_INVALID_ARG, "plans must be non-null");

@@ -77,6 +77,12 @@ namespace wsa {
 cudaError_t launch_plan_tables(const wsa_plan_s& p, cudaStream_t s);
 cudaError_t launch_transition(const wsa_plan_s& src, const wsa_plan_s& dst, const void* x_src,
                               void* x_dst, size_t row_bytes, cudaStream_t s);
+// Window-local 3D RoPE of one or two [n_rows, heads, head_dim] tensors (x[t]
+// -> y[t], in place allowed).  plan != null: video rows of the plan (canonical
+// or packed order); plan == null: text rows, token i at (i, i, i).
+cudaError_t launch_rope(const wsa_plan_s* plan, bool canonical, const void* const x[2], void* const y[2],
+                        int ntensors, int n_rows, int heads, int head_dim, bool bf16, int text_len, int rope_dim,
+                        double theta, cudaStream_t s);
 // y[i] = x[index[i]] for i < rows; rows whose index is outside [0, x_rows)
 // are skipped.
 cudaError_t launch_gather_rows(const void* x, int x_rows, const int* index, void* y, int rows, size_t row_bytes,
