@@ -89,3 +89,47 @@ def simulate(x_canonical, src, dst, ranks):
         recv = np.concatenate([send[r][bounds[r][d]:bounds[r][d + 1]] for r in range(ranks)])
         out.append(recv[sched["recv_index"][d]])
     return out, sched
+
+
+def plan_b(regular, shifted, ranks):
+    """Plan B (halo exchange) counts for one regular/shifted layer pair.
+
+    The pages name Plan B only as the follow-up to Plan A ("Limitations":
+    Plan A re-shards the full activation at every boundary; a halo exchange
+    needs its own crossover evaluation).  Reading used here:
+    * hidden rows stay with the regular layout's LPT owners for the whole
+      network, so regular layers exchange nothing;
+    * shifted window w is computed by the rank that holds most of its rows
+      (ties: lowest rank id); its other rows travel to that rank (halo in)
+      and their attention outputs travel back to their owners (halo out).
+
+    Returns a dict: owner of every shifted window, per-rank rows received
+    (halo_in) and sent (halo_out) before a shifted layer (the return trip
+    mirrors them), and per-rank shifted-layer work (sum of n_w and n_w^2)."""
+    own_r = owners(regular, ranks)
+    holder = np.empty(regular.num_tokens, dtype=np.int64)
+    for w in range(regular.num_windows):
+        holder[regular.ids[regular.offsets[w]:regular.offsets[w + 1]]] = own_r[w]
+    comp = np.empty(shifted.num_windows, dtype=np.int64)
+    halo_in = np.zeros(ranks, dtype=np.int64)
+    halo_out = np.zeros(ranks, dtype=np.int64)
+    tokens = np.zeros(ranks, dtype=np.int64)
+    work = np.zeros(ranks, dtype=np.float64)
+    for w in range(shifted.num_windows):
+        rows = shifted.ids[shifted.offsets[w]:shifted.offsets[w + 1]]
+        share = np.bincount(holder[rows], minlength=ranks)
+        r = int(np.argmax(share))  # first maximum: lowest rank id on ties
+        comp[w] = r
+        n = rows.size
+        halo_in[r] += n - share[r]
+        halo_out += share
+        halo_out[r] -= share[r]
+        tokens[r] += n
+        work[r] += float(n) * n
+    return {"owner": comp, "halo_in": halo_in, "halo_out": halo_out, "tokens": tokens, "work": work}
+
+
+def plan_a_rows_moved(src, dst, ranks):
+    """Rows that change rank at one Plan A boundary (off-diagonal sum of C)."""
+    c = plan_a(src, dst, ranks)["counts"]
+    return int(c.sum() - np.trace(c))

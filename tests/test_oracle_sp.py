@@ -88,3 +88,61 @@ def test_owner_hand_example():
     loads = [n[own == r].sum() for r in range(2)]
     assert sum(loads) == 576 and abs(loads[0] - loads[1]) <= n.max()
     assert own[0] == 0 and own[1] == 1  # the two largest windows (ties by id) go to ranks 0, 1
+
+
+# ---- Plan B (halo exchange) evaluation counts -------------------------------
+
+def _brute_plan_b(reg, sft, ranks):
+    # independent restatement: for each shifted window, count rows by holder
+    own = sp.owners(reg, ranks)
+    holder = {}
+    for w in range(reg.num_windows):
+        for c in reg.ids[reg.offsets[w]:reg.offsets[w + 1]]:
+            holder[int(c)] = int(own[w])
+    moved, comp = 0, []
+    for w in range(sft.num_windows):
+        rows = [int(c) for c in sft.ids[sft.offsets[w]:sft.offsets[w + 1]]]
+        counts = [sum(1 for c in rows if holder[c] == r) for r in range(ranks)]
+        best = max(range(ranks), key=lambda r: (counts[r], -r))
+        comp.append(best)
+        moved += len(rows) - counts[best]
+    return moved, comp
+
+
+@pytest.mark.parametrize("grid", GRIDS)
+@pytest.mark.parametrize("ranks", [1, 2, 3, 5])
+def test_plan_b_against_brute_force(grid, ranks):
+    reg, sft = oracle.make_plan(*grid, 0), oracle.make_plan(*grid, 1)
+    got = sp.plan_b(reg, sft, ranks)
+    moved, comp = _brute_plan_b(reg, sft, ranks)
+    assert list(got["owner"]) == comp
+    assert got["halo_in"].sum() == moved == got["halo_out"].sum()
+    assert got["tokens"].sum() == reg.num_tokens
+    assert got["work"].sum() == pytest.approx(float(np.sum(np.diff(sft.offsets).astype(np.float64) ** 2)))
+
+
+def test_plan_b_one_rank_and_one_window_move_nothing():
+    reg, sft = oracle.make_plan(21, 45, 80, 4, 3, 3, 0), oracle.make_plan(21, 45, 80, 4, 3, 3, 1)
+    assert sp.plan_b(reg, sft, 1)["halo_in"].sum() == 0
+    g = (2, 3, 4, 1, 1, 1)  # a single window in both layouts
+    assert sp.plan_b(oracle.make_plan(*g, 0), oracle.make_plan(*g, 1), 4)["halo_in"].sum() == 0
+
+
+def test_plan_b_hand_example():
+    # (T, H, W) = (1, 45, 80) at scale 1 with nw = 4: windows 45 x 20 columns.
+    # Regular column cuts 0,20,40,60,80 -> LPT over 2 ranks (all 900 tokens,
+    # ties to the lower rank): r0, r1, r0, r1.  Shifted cuts move by 10 on w
+    # only (H equals its window): 0,10,30,50,70,80.  Windows [10,30), [30,50)
+    # and [50,70) straddle two owners with 450 rows each -> computed by r0
+    # (tie), 450 halo rows each; [0,10) is r0's, [70,80) is r1's.
+    reg, sft = oracle.make_plan(1, 45, 80, 1, 1, 4, 0), oracle.make_plan(1, 45, 80, 1, 1, 4, 1)
+    assert [b[4:] for b in sft.boxes] == [(0, 10), (10, 30), (30, 50), (50, 70), (70, 80)]
+    got = sp.plan_b(reg, sft, 2)
+    assert list(got["owner"]) == [0, 0, 0, 0, 1]
+    assert list(got["halo_in"]) == [1350, 0] and list(got["halo_out"]) == [0, 1350]
+    assert list(got["tokens"]) == [3150, 450]
+    assert list(got["work"]) == [450.0 ** 2 + 3 * 900.0 ** 2, 450.0 ** 2]
+    # Plan A: shifted LPT sizes 450,900,900,900,450 -> owners r1,r0,r1,r0,r1;
+    # columns 0-9, 20-29, 40-49 and 60-69 change rank: 4 x 450 rows.
+    assert list(sp.owners(sft, 2)) == [1, 0, 1, 0, 1]
+    assert sp.plan_a_rows_moved(reg, sft, 2) == 1800
