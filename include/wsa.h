@@ -302,6 +302,29 @@ wsa_status wsa_sp_plan_a(int T, int H, int W, int nt, int nh, int nw,
                          int* n_recv, int* network_exchange_required);
 
 /*
+ * wsa_sp_plan_b -- host only: the counts of a Plan B halo exchange for one
+ * regular/shifted layer pair, for the crossover evaluation against Plan A.
+ * The note leaves Plan B to a follow-up ("Window-Aligned Sequence
+ * Parallelism (SeedVR2)", section "Limitations"); this call reads it as:
+ *   - hidden rows stay with the regular layout's LPT owners (as in
+ *     wsa_sp_owners) for the whole network, so regular layers exchange
+ *     nothing;
+ *   - shifted window w is computed by the rank holding most of its rows
+ *     (window_rank[w]; the lowest rank id on ties);
+ *   - its other rows travel to that rank before the shifted layer (halo_in
+ *     of the receiver, halo_out of each sender), and their outputs travel
+ *     back after it (the same counts, mirrored).
+ * Outputs (each may be NULL): window_rank [num_windows of the shifted
+ * layout]; halo_in, halo_out, tokens (sum of n_w of the windows a rank
+ * computes) and work (sum of n_w^2) [ranks each].  *num_windows is always
+ * written.  A window_rank capacity below the count is WSA_ERR_INVALID_ARG.
+ */
+wsa_status wsa_sp_plan_b(int T, int H, int W, int nt, int nh, int nw,
+                         int max_temporal, int ranks, int* window_rank,
+                         int capacity, int* num_windows, long long* halo_in,
+                         long long* halo_out, long long* tokens, double* work);
+
+/*
  * wsa_gather_rows -- y[i] = x[index[i]] for 0 <= i < rows: the pack
  * (index = send_index) and unpack (index = recv_index) steps of the Plan A
  * exchange, on the device.

@@ -64,6 +64,8 @@ def _load():
         "wsa_sp_plan_a": ([i] * 11 + [ctypes.POINTER(ctypes.c_longlong), ip, i, ip, i, ip, ip, ip], i),
         "wsa_gather_rows": ([p, i, p, p, i, i, i, p], i),
         "wsa_rope": ([p, p, p, p, p, i, i, i, i, i, i, f, p], i),
+        "wsa_sp_plan_b": ([i] * 8 + [ip, i, ip] + [ctypes.POINTER(ctypes.c_longlong)] * 3
+                          + [ctypes.POINTER(ctypes.c_double)], i),
         "wsa_rope_text": ([p, p, p, p, i, i, i, i, i, f, p], i),
     }
     for name, (args, res) in sigs.items():

@@ -52,6 +52,7 @@ constexpr int kSlots = 5;                   // K/V ring slots
 constexpr int kLoaderWarp0 = 8;
 constexpr int kLoaderWarps = 2;
 constexpr int kLoaderRows = kTile / kLoaderWarps;  // 64 rows of each tile per gather warp
+constexpr int kIdsPerLane = kLoaderRows / 32;      // row ids a lane holds for one tile
 constexpr int kMmaWarp = kLoaderWarp0 + kLoaderWarps;
 constexpr int kSchedWarp = kMmaWarp + 1;
 constexpr int kThreads = (kSchedWarp + 1) * 32;     // 12 warps: 3 per SM sub-partition
@@ -349,12 +350,12 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
   auto acquire = [&](uint32_t bar, uint32_t parity, int code) -> bool {
     return __all_sync(0xffffffffu, wait_bar(bar, parity, err, code));
   };
-  // lane l holds the source rows of rows kLoaderRows*lw + l and + 32 + l of
-  // segment tile j (-1: past the end of its part, zero fill): a video row id
-  // for the first nvt tiles, a text row index for the text tiles after them.
-  auto fetch_ids = [&](int (&ids)[2], int j, int nv, int nvt, int off) {
+  // lane l holds the source rows of rows kLoaderRows*lw + 32*h + l of segment
+  // tile j (-1: past the end of its part, zero fill): a video row id for the
+  // first nvt tiles, a text row index for the text tiles after them.
+  auto fetch_ids = [&](int (&ids)[kIdsPerLane], int j, int nv, int nvt, int off) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kIdsPerLane; ++h) {
       const int lr = kLoaderRows * lw + 32 * h + lane;
       ids[h] = -1;
       if (!kText || j < nvt) {
@@ -366,17 +367,17 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
       }
     }
   };
-  auto copy_tile = [&](const char* src, uint32_t dst, const int (&ids)[2], int head) {
+  auto copy_tile = [&](const char* src, uint32_t dst, const int (&ids)[kIdsPerLane], int head) {
     const char* colbase = src + static_cast<long long>(head) * (kD * 2) + chunk * 16;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < kLoaderRows / 2; ++i) {
       const int r = kLoaderRows * lw + half + 2 * i;
       const int id = __shfl_sync(0xffffffffu, ids[i >> 4], half + 2 * (i & 15));
       const char* g = id >= 0 ? colbase + static_cast<long long>(id) * prm.row_stride : src;
       cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
     }
   };
-  auto load_kv = [&](const int (&ids)[2], int head, bool text) -> bool {  // text: a text tile
+  auto load_kv = [&](const int (&ids)[kIdsPerLane], int head, bool text) -> bool {  // text: a text tile
     for (int which = 0; which < 2; ++which) {
       const uint32_t slot = ring_iter % kSlots;
       if (!acquire(bar_at(sm, B_RING_EMPTY + slot), ((ring_iter / kSlots) & 1) ^ 1, E_LOAD_RING_EMPTY))
@@ -400,7 +401,7 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     const int nkv = nvt + (kText ? (prm.n_text + kTile - 1) / kTile : 0);
     const int qt0 = q0 / kTile;
     const bool has1 = qt0 + 1 < nkv;
-    int ids[2], ids_next[2], qids0[2], qids1[2];
+    int ids[kIdsPerLane], ids_next[kIdsPerLane], qids0[kIdsPerLane], qids1[kIdsPerLane];
     fetch_ids(ids, 0, nv, nvt, off);
     fetch_ids(qids0, qt0, nv, nvt, off);
     if (has1) fetch_ids(qids1, qt0 + 1, nv, nvt, off);
@@ -414,8 +415,8 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     cp_async_arrive(bar_at(sm, B_Q_FULL));
     bool ok = true;
     for (int j = 1; j < nkv && ok; ++j) {
-      ids[0] = ids_next[0];
-      ids[1] = ids_next[1];
+#pragma unroll
+      for (int h = 0; h < kIdsPerLane; ++h) ids[h] = ids_next[h];
       if (j + 1 < nkv) fetch_ids(ids_next, j + 1, nv, nvt, off);
       ok = load_kv(ids, head, j >= nvt);
     }

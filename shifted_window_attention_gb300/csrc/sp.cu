@@ -14,6 +14,14 @@
 //   in order with one argsort of their destination positions.  Whether any
 //   row crosses ranks is decided from the global C.
 //
+// Plan B (wsa_sp_plan_b) is the halo-exchange alternative that the note
+// leaves to a separate crossover evaluation ("Limitations").  This library
+// reads it as follows.  Hidden rows stay with the regular layout's owners,
+// and each shifted window is computed by the rank holding most of its rows.
+// The other rows travel to that rank before the shifted layer, and their
+// outputs travel back after it.  The call returns the counts that the
+// evaluation compares with Plan A.
+//
 // The planner needs no GPU and costs O(N) per call.  The receiver's argsort
 // is computed by counting: the destination positions are distinct, so
 // argsort[p] is the receive-buffer row that holds destination position p.
@@ -215,6 +223,48 @@ wsa_status wsa_sp_plan_a(int T, int H, int W, int nt, int nh, int nw, wsa_layout
     for (int w = 0; w < D.num_windows(); ++w)
       if (own_d[w] == rank)
         D.for_each_id(w, [&](int id) { recv_index[p++] = static_cast<int>(next[src_rank[id]]++); });
+  }
+  return WSA_OK;
+}
+
+wsa_status wsa_sp_plan_b(int T, int H, int W, int nt, int nh, int nw, int max_temporal, int ranks,
+                         int* window_rank, int capacity, int* num_windows, long long* halo_in, long long* halo_out,
+                         long long* tokens, double* work) {
+  if (!num_windows) return fail(WSA_ERR_INVALID_ARG, "num_windows is null");
+  if (ranks <= 0) return fail(WSA_ERR_INVALID_ARG, "ranks must be > 0");
+  Layout R, S;
+  wsa_status st = make_layout(T, H, W, nt, nh, nw, WSA_REGULAR, max_temporal, &R);
+  if (st != WSA_OK) return st;
+  st = make_layout(T, H, W, nt, nh, nw, WSA_SHIFTED, max_temporal, &S);
+  if (st != WSA_OK) return st;
+  *num_windows = S.num_windows();
+  if (window_rank && capacity < S.num_windows())
+    return fail(WSA_ERR_INVALID_ARG, "window_rank capacity is smaller than the shifted window count");
+  const std::vector<int> own = lpt_owner(R, ranks);
+  std::vector<int> holder, unused;
+  std::vector<long long> held;
+  assign_rows(R, own, ranks, &holder, &unused, &held);
+  std::vector<long long> in(ranks, 0), out(ranks, 0), tok(ranks, 0), share(ranks, 0);
+  std::vector<double> wk(ranks, 0.0);
+  for (int w = 0; w < S.num_windows(); ++w) {
+    std::fill(share.begin(), share.end(), 0);
+    S.for_each_id(w, [&](int id) { ++share[holder[id]]; });
+    int best = 0;  // the rank holding most rows; the lowest id on ties
+    for (int r = 1; r < ranks; ++r)
+      if (share[r] > share[best]) best = r;
+    const long long n = S.window_tokens(w);
+    in[best] += n - share[best];
+    for (int r = 0; r < ranks; ++r)
+      if (r != best) out[r] += share[r];
+    tok[best] += n;
+    wk[best] += static_cast<double>(n) * static_cast<double>(n);
+    if (window_rank) window_rank[w] = best;
+  }
+  for (int r = 0; r < ranks; ++r) {
+    if (halo_in) halo_in[r] = in[r];
+    if (halo_out) halo_out[r] = out[r];
+    if (tokens) tokens[r] = tok[r];
+    if (work) work[r] = wk[r];
   }
   return WSA_OK;
 }

@@ -116,4 +116,104 @@ class PlanA:
             raise WsaError(-1, f"expected [{n}, channels] rows, got {tuple(x.shape)}")
 
 
-__all__ = ["owners", "local_rows", "PlanA"]
+__all__ = ["owners", "local_rows", "PlanA", "plan_b", "crossover"]
+
+
+def plan_b(T, H, W, nt, nh, nw, ranks, max_temporal=30):
+    """wsa_sp_plan_b: Plan B halo-exchange counts for one regular/shifted
+    layer pair (host only).  Returns a dict of numpy arrays: ``window_rank``
+    (computing rank of every shifted window), ``halo_in``, ``halo_out``,
+    ``tokens`` and ``work`` per rank."""
+    n = ctypes.c_int()
+    _check(lib.wsa_sp_plan_b(T, H, W, nt, nh, nw, max_temporal, ranks, None, 0, ctypes.byref(n),
+                             None, None, None, None))
+    wr = np.zeros(n.value, dtype=np.int32)
+    arrs = {k: np.zeros(ranks, dtype=np.int64) for k in ("halo_in", "halo_out", "tokens")}
+    work = np.zeros(ranks, dtype=np.float64)
+    ll = ctypes.POINTER(ctypes.c_longlong)
+    _check(lib.wsa_sp_plan_b(T, H, W, nt, nh, nw, max_temporal, ranks,
+                             wr.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n.value, ctypes.byref(n),
+                             arrs["halo_in"].ctypes.data_as(ll), arrs["halo_out"].ctypes.data_as(ll),
+                             arrs["tokens"].ctypes.data_as(ll), work.ctypes.data_as(ctypes.POINTER(ctypes.c_double))))
+    return {"window_rank": wr, "work": work, **arrs}
+
+
+def crossover(T, H, W, nt, nh, nw, ranks, channels, bytes_per_elem=2, max_temporal=30, shifted_ms=None):
+    """The Plan A / Plan B comparison for one regular + shifted layer pair.
+
+    Plan A moves the rows that change rank at both boundaries (off-diagonal
+    counts of each wsa_sp_plan_a matrix).  Plan B moves the halo rows in and
+    their outputs back around the shifted layer.  Rows count as hidden-state
+    rows of ``channels`` elements.  Also reported: the busiest rank's traffic
+    (it bounds the all-to-all time) and the attention work imbalance of the
+    shifted layer (max over mean of sum n_w^2; Plan A balances it by LPT on
+    tokens).
+
+    With ``shifted_ms``, the measured one-GPU time of the shifted attention
+    layer, the busiest rank's attention time is estimated under each plan as
+    shifted_ms times its share of the total sum of n_w^2.  The result then
+    includes the link bandwidth below which Plan B's smaller exchange
+    outweighs its imbalance: the difference in the busiest rank's bytes
+    divided by the difference in the busiest rank's attention time."""
+    row = channels * bytes_per_elem
+    a_rows, a_max = 0, 0
+    for src, dst in ((0, 1), (1, 0)):
+        c = PlanA(T, H, W, nt, nh, nw, src, dst, ranks, 0, max_temporal).counts
+        off = c - np.diag(np.diag(c))
+        a_rows += int(off.sum())
+        a_max += int(max(off.sum(axis=1).max(), off.sum(axis=0).max()))
+    b = plan_b(T, H, W, nt, nh, nw, ranks, max_temporal)
+    b_rows = 2 * int(b["halo_in"].sum())
+    b_max = 2 * int(max(b["halo_in"].max(), b["halo_out"].max()))
+    # Plan A's shifted-layer work per rank under its own LPT assignment
+    own = owners(T, H, W, nt, nh, nw, 1, ranks, max_temporal)
+    n = np.array([(b1 - b0) * (h1 - h0) * (w1 - w0) for (b0, b1, h0, h1, w0, w1) in
+                  _boxes(T, H, W, nt, nh, nw, 1, max_temporal)], dtype=np.float64)
+    a_work = np.bincount(own, weights=n * n, minlength=ranks)
+    extra = {}
+    if shifted_ms is not None:
+        total = float(a_work.sum())
+        ta = shifted_ms * float(a_work.max()) / total
+        tb = shifted_ms * float(b["work"].max()) / total
+        dbytes = (a_max - b_max) * row
+        extra = {"plan_a_shifted_ms_max_rank": ta, "plan_b_shifted_ms_max_rank": tb,
+                 "crossover_link_gbs": dbytes / ((tb - ta) * 1e-3) / 1e9 if tb > ta and dbytes > 0 else None}
+    return {
+        **extra,
+        "ranks": ranks,
+        "plan_a_bytes": a_rows * row, "plan_a_max_rank_bytes": a_max * row,
+        "plan_b_bytes": b_rows * row, "plan_b_max_rank_bytes": b_max * row,
+        "plan_a_shifted_imbalance": float(a_work.max() / a_work.mean()),
+        "plan_b_shifted_imbalance": float(b["work"].max() / b["work"].mean()),
+    }
+
+
+def _boxes(T, H, W, nt, nh, nw, layout, max_temporal):
+    from . import layout_windows
+    return layout_windows(T, H, W, nt, nh, nw, layout, max_temporal)
+
+
+def _main():
+    import argparse
+    ap = argparse.ArgumentParser(description="Plan A / Plan B exchange comparison for one layer pair")
+    ap.add_argument("grid", type=int, nargs=6, metavar=("T", "H", "W", "nt", "nh", "nw"))
+    ap.add_argument("--channels", type=int, default=3072)
+    ap.add_argument("--ranks", type=int, nargs="+", default=[2, 4, 8])
+    ap.add_argument("--shifted-ms", type=float, default=None,
+                    help="measured one-GPU time of the shifted attention layer (ms)")
+    args = ap.parse_args()
+    for r in args.ranks:
+        c = crossover(*args.grid, r, args.channels, shifted_ms=args.shifted_ms)
+        line = (f"ranks {r}: Plan A {c['plan_a_bytes'] / 1e6:.1f} MB (busiest rank "
+                f"{c['plan_a_max_rank_bytes'] / 1e6:.1f}), Plan B {c['plan_b_bytes'] / 1e6:.1f} MB (busiest rank "
+                f"{c['plan_b_max_rank_bytes'] / 1e6:.1f}); shifted-layer work imbalance A "
+                f"{c['plan_a_shifted_imbalance']:.3f}, B {c['plan_b_shifted_imbalance']:.3f}")
+        if args.shifted_ms is not None:
+            x = c["crossover_link_gbs"]
+            line += (f"; Plan B wins only on links slower than {x:.0f} GB/s" if x
+                     else "; Plan B never wins (its busiest rank also moves more bytes)")
+        print(line)
+
+
+if __name__ == "__main__":
+    _main()

@@ -98,3 +98,37 @@ def test_errors(sp):
     assert lib.wsa_gather_rows(None, 0, None, None, 0, 8, 0, None) == 0   # rows == 0: no-op
     assert lib.wsa_gather_rows(None, 4, None, None, 4, 8, 0, None) == -1  # null pointers
     assert lib.wsa_gather_rows(None, 4, None, None, 4, 0, 0, None) == -1  # channels
+
+
+@pytest.mark.parametrize("name", list(GRIDS))
+@pytest.mark.parametrize("ranks", [1, 2, 3, 8])
+def test_plan_b_matches_oracle(sp, name, ranks):
+    grid = GRIDS[name]
+    ref = osp.plan_b(oracle.make_plan(*grid, 0), oracle.make_plan(*grid, 1), ranks)
+    got = sp.plan_b(*grid, ranks)
+    assert np.array_equal(got["window_rank"], ref["owner"])
+    for k in ("halo_in", "halo_out", "tokens"):
+        assert np.array_equal(got[k], ref[k]), k
+    assert np.array_equal(got["work"], ref["work"])
+
+
+def test_crossover_hand_grid(sp):
+    # the hand-worked grid of the oracle pin: Plan A moves 1800 rows at each of
+    # the two boundaries, Plan B 1350 halo rows in and 1350 outputs back.
+    c = sp.crossover(1, 45, 80, 1, 1, 4, 2, channels=3072)
+    row = 3072 * 2
+    assert c["plan_a_bytes"] == 2 * 1800 * row
+    assert c["plan_b_bytes"] == 2 * 1350 * row
+    assert c["plan_b_max_rank_bytes"] == 2 * 1350 * row
+    assert c["plan_b_shifted_imbalance"] > c["plan_a_shifted_imbalance"]
+
+
+def test_plan_b_errors(sp):
+    import ctypes
+    from shifted_window_attention_gb300 import WsaError
+    with pytest.raises(WsaError, match="INVALID_ARG"):
+        sp.plan_b(*GRIDS["tiny"], 0)
+    n = ctypes.c_int()
+    small = (ctypes.c_int * 2)()
+    assert sp.lib.wsa_sp_plan_b(*GRIDS["tiny"], 30, 2, small, 2, ctypes.byref(n), None, None, None, None) == -1
+    assert n.value == 36
