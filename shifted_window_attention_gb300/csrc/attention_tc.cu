@@ -56,7 +56,7 @@ constexpr int kIdsPerLane = kLoaderRows / 32;      // row ids a lane holds for o
 constexpr int kMmaWarp = kLoaderWarp0 + kLoaderWarps;
 constexpr int kSchedWarp = kMmaWarp + 1;
 constexpr int kThreads = (kSchedWarp + 1) * 32;     // 12 warps: 3 per SM sub-partition
-constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleLog2 = 24.0f;  // p <= 2^24; row sums <= 2^36, far inside fp32
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
 
 enum : int {
