@@ -164,6 +164,12 @@ def run_ours(args):
     # than 4 layers cycle 4 seeded input sets (the values do not change the work).
     n_sets = min(L, 4)
     sets = [wsa_inputs.qkv(wl, layer=i, device=dev) for i in range(n_sets)]
+    canonical = not args.packed
+    if args.packed:
+        # rows in the plan-packed order of each set's layout (untimed setup)
+        for i in range(n_sets):
+            ids = plans[i % 2].tables()[2].long()
+            sets[i] = tuple(t[ids].contiguous() for t in sets[i])
     outs = [torch.empty_like(sets[i % n_sets][0]) for i in range(min(L, 2))]
     n_text = args.text
     if n_text:
@@ -183,6 +189,8 @@ def run_ours(args):
     trans_bytes = 2.0 * N * C * 2 + 2 * 4.0 * N  # read + write rows, two int32 table reads
 
     use_rope = args.rope >= 0
+    if use_rope and args.packed:
+        raise SystemExit("--rope is timed on canonical rows only")
     if use_rope:
         # rotated Q/K of the current layer (window-local positions of its layout)
         qk_rot = [(torch.empty_like(sets[0][0]), torch.empty_like(sets[0][1])) for _ in range(2)]
@@ -213,7 +221,7 @@ def run_ours(args):
                 wsa.attention_text(plans[l % 2], q, k, v, qt, kt, vt, out=outs[l % 2],
                                    out_txt=touts[l % 2], workspace=wspace[l % 2])
             else:
-                wsa.attention(plans[l % 2], q, k, v, out=outs[l % 2])
+                wsa.attention(plans[l % 2], q, k, v, out=outs[l % 2], canonical=canonical)
             if e: e[4 * l + 2].record(stream)
             if l + 1 < L:
                 wsa.transition(plans[l % 2], plans[(l + 1) % 2], hidden[l % 2], out=hidden[(l + 1) % 2])
@@ -267,9 +275,9 @@ def run_ours(args):
         def e2e_step():
             for d_, h_ in zip(dev_in, host_in):
                 d_.copy_(h_, non_blocking=True)
-            wsa.attention(plans[0], q0, k0, v0, out=outs[0])
+            wsa.attention(plans[0], q0, k0, v0, out=outs[0], canonical=canonical)
             wsa.transition(plans[0], plans[1], x, out=y)
-            wsa.attention(plans[1], q1, k1, v1, out=outs[1])
+            wsa.attention(plans[1], q1, k1, v1, out=outs[1], canonical=canonical)
             for h_, d_ in zip(host_out, (outs[0], outs[1], y)):
                 h_.copy_(d_, non_blocking=True)
 
@@ -291,7 +299,7 @@ def run_ours(args):
     traffic, traffic_note = None, "no ncu capture for this kernel source / workload"
     mt = MEASURED_TRAFFIC
     if (kernel_sha1() == mt["kernel_sha1"] and wl.name == mt["workload"] and wl.heads == mt["heads"]
-            and not n_text):
+            and not n_text and not args.packed):
         traffic = mt["bytes"]
         traffic_note = ("DRAM bytes of the regular-layout launch (ncu capture of the 8-head case scaled x3); "
                         f"algorithmic {4.0 * N * wl.channels * 2:.3e} B")
@@ -335,7 +343,10 @@ def run_ours(args):
         "data": f"synthetic (seeded torch.randn, {dist_note}, bf16)",
         "config": {"workload": f"{wl.name}: T={wl.T},H={wl.H},W={wl.W} ({N} tokens), nt,nh,nw={wl.nt},{wl.nh},{wl.nw} "
                                f"-> wt,wh,ww={plans[0].wt},{plans[0].wh},{plans[0].ww}; {wl.heads} heads x {wl.head_dim}; "
-                               f"{L} alternating layers (attention gathers/scatters through ids) with "
+                               f"{L} alternating layers ("
+                               + ("attention on rows in plan-packed order, full tiles by TMA" if args.packed
+                                  else "attention gathers/scatters through ids")
+                               + f") with "
                                f"{L - 1} transitions of [N,{C}]"
                                + (f"; segments [window, {n_text} text tokens], text mean over windows" if n_text else "")
                                + (f"; window-local 3D RoPE of Q/K (text_len {args.rope}) before each attention"
@@ -528,6 +539,9 @@ def main():
     ap.add_argument("--text", type=int, default=0, help="replicated text tokens appended to every window segment")
     ap.add_argument("--rope", type=int, default=-1,
                     help="apply window-local 3D RoPE to Q/K before every attention, with this text_len (>= 0)")
+    ap.add_argument("--packed", action="store_true",
+                    help="attention on Q/K/V rows in plan-packed order (what the transition produces) instead of "
+                         "canonical rows gathered through ids")
     ap.add_argument("--plan-a", type=int, default=0,
                     help="time the Plan A pack/unpack kernels for this many emulated ranks instead")
     args = ap.parse_args()

@@ -117,7 +117,11 @@ wsa_status wsa_plan_tables(wsa_plan_t plan, const int** offsets, const int** dim
  *   then channels).  in_order_canonical = 1: row = canonical token id;
  *   0: row = packed position of the plan (what wsa_transition produces).
  *   The window gather and the output scatter go through the plan's ids table
- *   inside the kernel; no separate permutation pass runs.
+ *   inside the kernel; no separate permutation pass runs.  With packed rows
+ *   (bf16) a window's full 128-row tiles are plain strided blocks and arrive
+ *   by TMA tile loads; its last partial tile is gathered with zero fill, so
+ *   rows of another window never enter its tiles.  Both orders give
+ *   bit-identical results.
  * dtype WSA_BF16: head_dim must be 128; tensor-core kernel (tcgen05, TMEM),
  *   fp32 accumulation and softmax, bf16 output; pointers 16-byte aligned.
  * dtype WSA_FP32: head_dim 64 or 128; fp32 CUDA-core kernel throughout.

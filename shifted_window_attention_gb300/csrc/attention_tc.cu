@@ -19,14 +19,19 @@
 //    Q/K/V rows with 16-byte cp.async into 128B-swizzled shared-memory tiles;
 //    one thread of warp 10 issues every tcgen05.mma, and one thread of warp 11
 //    takes work units from the global counter up to two units ahead.
+//  * Rows in plan-packed order: a full 128-row tile of a window is a plain
+//    strided block of the [N, heads, 128] tensor, so it arrives by two TMA
+//    tile loads (cp.async.bulk.tensor, one per 64-channel panel, the same
+//    128-byte swizzle).  A window's last, partial tile is still gathered with
+//    zero fill, so no row of another window ever enters a tile.
 //  * TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The bf16
 //    probabilities P overwrite the first 64 columns of their S tile and feed
 //    the P V product straight from TMEM (A operand in TMEM); V is the B
 //    operand, read MN-major from shared memory.
 //  * Online softmax in the log2 domain with a lazy rescale: the running max is
 //    only raised (and O rescaled in TMEM) when a row's max grows by more than
-//    2^8, which keeps every probability <= 256 and the result exact up to
-//    rounding.  The row sum accumulates the same bf16-rounded probabilities
+//    24 (log2), which keeps every probability <= 2^24 and the result exact up
+//    to rounding.  The row sum accumulates the same bf16-rounded probabilities
 //    that enter the P V product.
 //  * Output rows leave TMEM through registers with 256-bit stores when the
 //    output is 32-byte aligned.
@@ -34,10 +39,12 @@
 //    plan's workspace and the CTA unwinds, drains its MMAs and cp.asyncs and
 //    frees TMEM.
 
+#include <cuda.h>  // CUtensorMap and its encoder's types (the encoder is reached through the runtime)
 #include <cuda_bf16.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 
 #include "wsa_internal.h"
 
@@ -58,6 +65,7 @@ constexpr int kSchedWarp = kMmaWarp + 1;
 constexpr int kThreads = (kSchedWarp + 1) * 32;     // 12 warps: 3 per SM sub-partition
 constexpr float kRescaleLog2 = 24.0f;  // p <= 2^24; row sums <= 2^36, far inside fp32
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+constexpr long long kTmaDrainCycles = 400000LL;  // ~0.2 ms: TMA loads in flight after an error
 
 enum : int {
   B_RING_FULL = 0,
@@ -98,6 +106,9 @@ enum : int {
 };
 
 struct TcParams {
+  // Tile maps of q, k, v as [N rows][heads][128] bf16, box 64 channels x 1
+  // head x 128 rows, 128-byte swizzle (set only for the packed-order TMA path).
+  CUtensorMap tm_q, tm_k, tm_v;
   const char* q;
   const char* k;
   const char* v;
@@ -171,6 +182,20 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* err
       }
     }
   }
+}
+
+// Raises the transaction count the barrier's current phase waits for (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// TMA tile load of box (x, y, z) of a 3-D tensor map into shared memory; the
+// landed bytes complete transactions on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -338,7 +363,11 @@ __device__ __forceinline__ uint32_t bar_at(const Smem& s, int i) { return s.bars
 // gather warps never wait for data; the MMA thread makes the landed rows
 // visible to the tensor core with a proxy fence.  The token ids of the next
 // key tile are fetched while the current one is issued.
-template <bool kText>
+// kTma (packed rows, no text): full tiles come by TMA instead.  Lane 0 of
+// gather warp 0 raises the barrier's transaction count by the tile's bytes
+// and issues the two panel loads; every lane still makes its usual arrival,
+// so the barrier counts are the same for both kinds of tile.
+template <bool kText, bool kTma>
 __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm, int lw, int lane) {
   int* err = prm.work + WS_ERROR;
   const int half = lane >> 4;
@@ -377,17 +406,34 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
       cp_async16(dst + panel_off + r * 128 + ((cc ^ (r & 7)) << 4), g, id >= 0 ? 16u : 0u);
     }
   };
-  auto load_kv = [&](const int (&ids)[kIdsPerLane], int head, bool text) -> bool {  // text: a text tile
+  const bool tma_lane = kTma && lw == 0 && lane == 0;
+  // Both panels of the packed rows [row, row + 128) of `head` (TMA path only).
+  auto tma_tile = [&](const CUtensorMap* map, uint32_t dst, int row, int head, uint32_t bar) {
+    mbar_expect_tx(bar, kTileBytes);
+    tma_load_3d(dst, map, 0, head, row, bar);
+    tma_load_3d(dst + kPanelBytes, map, 64, head, row, bar);
+  };
+  // text: a text tile; tma_row >= 0: a full tile of packed rows from that row
+  auto load_kv = [&](const int (&ids)[kIdsPerLane], int head, bool text, int tma_row) -> bool {
     for (int which = 0; which < 2; ++which) {
       const uint32_t slot = ring_iter % kSlots;
       if (!acquire(bar_at(sm, B_RING_EMPTY + slot), ((ring_iter / kSlots) & 1) ^ 1, E_LOAD_RING_EMPTY))
         return false;
-      copy_tile(kText && text ? (which ? prm.vt : prm.kt) : (which ? prm.v : prm.k), sm.ring + slot * kTileBytes, ids,
-                head);
-      cp_async_arrive(bar_at(sm, B_RING_FULL + slot));
+      const uint32_t full = bar_at(sm, B_RING_FULL + slot);
+      if (kTma && tma_row >= 0) {
+        if (tma_lane) tma_tile(which ? &prm.tm_v : &prm.tm_k, sm.ring + slot * kTileBytes, tma_row, head, full);
+      } else {
+        copy_tile(kText && text ? (which ? prm.vt : prm.kt) : (which ? prm.v : prm.k), sm.ring + slot * kTileBytes,
+                  ids, head);
+      }
+      cp_async_arrive(full);
       ++ring_iter;
     }
     return true;
+  };
+  // Packed row of tile j when it is a full tile loaded by TMA, else -1.
+  auto tma_row_of = [&](int j, int nv, int off) -> int {
+    return kTma && (j + 1) * kTile <= nv ? off + j * kTile : -1;
   };
 
   while (true) {
@@ -408,17 +454,27 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     // K0/V0 first: they may land while the previous unit's last MMAs still
     // hold the Q buffers.
     if (nkv > 1) fetch_ids(ids_next, 1, nv, nvt, off);
-    if (!load_kv(ids, head, nvt == 0)) break;
+    if (!load_kv(ids, head, nvt == 0, tma_row_of(0, nv, off))) break;
     if (!acquire(bar_at(sm, B_Q_EMPTY), (unit_iter & 1) ^ 1, E_LOAD_Q_EMPTY)) break;
-    copy_tile(kText && qt0 >= nvt ? prm.qt : prm.q, sm.q0, qids0, head);
-    if (has1) copy_tile(kText && qt0 + 1 >= nvt ? prm.qt : prm.q, sm.q0 + kTileBytes, qids1, head);
-    cp_async_arrive(bar_at(sm, B_Q_FULL));
+    const uint32_t qfull = bar_at(sm, B_Q_FULL);
+    const int qrow0 = tma_row_of(qt0, nv, off), qrow1 = has1 ? tma_row_of(qt0 + 1, nv, off) : -1;
+    if (kTma && qrow0 >= 0) {
+      if (tma_lane) tma_tile(&prm.tm_q, sm.q0, qrow0, head, qfull);
+    } else {
+      copy_tile(kText && qt0 >= nvt ? prm.qt : prm.q, sm.q0, qids0, head);
+    }
+    if (kTma && qrow1 >= 0) {
+      if (tma_lane) tma_tile(&prm.tm_q, sm.q0 + kTileBytes, qrow1, head, qfull);
+    } else if (has1) {
+      copy_tile(kText && qt0 + 1 >= nvt ? prm.qt : prm.q, sm.q0 + kTileBytes, qids1, head);
+    }
+    cp_async_arrive(qfull);
     bool ok = true;
     for (int j = 1; j < nkv && ok; ++j) {
 #pragma unroll
       for (int h = 0; h < kIdsPerLane; ++h) ids[h] = ids_next[h];
       if (j + 1 < nkv) fetch_ids(ids_next, j + 1, nv, nvt, off);
-      ok = load_kv(ids, head, j >= nvt);
+      ok = load_kv(ids, head, j >= nvt, tma_row_of(j, nv, off));
     }
     if (!ok) break;
     __syncwarp();
@@ -426,6 +482,13 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     ++unit_iter;
   }
   cp_async_wait_all();
+  // After a failed wait, TMA loads this lane issued may still be landing and
+  // their barrier phases may never complete: give them a bounded time (a
+  // tile lands in microseconds) before the CTA releases its shared memory.
+  if (tma_lane && *reinterpret_cast<volatile int*>(err) != 0) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < kTmaDrainCycles) __nanosleep(1000);
+  }
 }
 
 // One thread hands out work units: it takes the next unit from the global
@@ -549,7 +612,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // One key tile of the online softmax for this thread's query row: reads the
 // 128 scores of S, updates the running max m (log2 domain, lazily) and the
 // running sum l2 (two partial sums), rescales O in TMEM when the max grows by
-// more than 2^8, and writes the bf16 probabilities P over the first 64
+// more than kRescaleLog2 (log2), and writes the bf16 probabilities P over the first 64
 // columns of S.  kFull: all 128 key columns are valid (no masking).
 template <bool kFull>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool first, int kv_valid, float c,
@@ -720,8 +783,8 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
 
 // Registers: each SM sub-partition holds 16K registers and 3 of the 12
 // warps, so 168 registers per thread fit (3 x 32 x 168 = 16,128).
-template <bool kText>
-__global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
+template <bool kText, bool kTma>
+__global__ void __maxnreg__(168) attention_tc_kernel(const __grid_constant__ TcParams prm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -763,7 +826,7 @@ __global__ void __maxnreg__(168) attention_tc_kernel(const TcParams prm) {
   if (warp < kLoaderWarp0) {
     softmax_role<kText>(prm, sm, tmem, warp, lane);
   } else if (warp < kMmaWarp) {
-    loader_role<kText>(prm, sm, warp - kLoaderWarp0, lane);
+    loader_role<kText, kTma>(prm, sm, warp - kLoaderWarp0, lane);
   } else if (warp == kMmaWarp) {
     if (lane == 0) mma_role<kText>(prm, sm, tmem);
   } else if (lane == 0) {
@@ -857,10 +920,57 @@ cudaError_t launch_attention_bf16_tc(const wsa_plan_s& p, const void* q, const v
                              p.d_tc_items, p.num_tc_items);
 }
 
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library itself); null if unavailable.
+EncodeTiled encoder() {
+  static const EncodeTiled fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiled>(nullptr);
+    return reinterpret_cast<EncodeTiled>(f);
+  }();
+  return fn;
+}
+
+// Tile map of a [rows, heads, 128] bf16 tensor: box of 64 channels x 1 head x
+// 128 rows, 128-byte swizzle, rows past the end read as zero.
+cudaError_t encode_rows(CUtensorMap* map, const void* base, int rows, int heads) {
+  const EncodeTiled enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(heads) * kD * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTile)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_attention_tc(const wsa_plan_s& p, const void* q, const void* k, const void* v, void* o, int heads,
                                 bool canonical, float scale, cudaStream_t s, const void* qt, const void* kt,
                                 const void* vt, float* text_part, int n_text, const WorkItem* items, int n_items) {
   TcParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  // Packed rows without a text segment: full tiles by TMA.
+  const bool tma = !canonical && n_text == 0;
+  if (tma) {
+    cudaError_t e = encode_rows(&prm.tm_q, q, p.num_tokens, heads);
+    if (e == cudaSuccess) e = encode_rows(&prm.tm_k, k, p.num_tokens, heads);
+    if (e == cudaSuccess) e = encode_rows(&prm.tm_v, v, p.num_tokens, heads);
+    if (e != cudaSuccess) return e;
+  }
   prm.q = static_cast<const char*>(q);
   prm.k = static_cast<const char*>(k);
   prm.v = static_cast<const char*>(v);
@@ -882,7 +992,8 @@ cudaError_t launch_attention_tc(const wsa_plan_s& p, const void* q, const void* 
   prm.work = p.d_work;
   // The text segment is a separate instantiation: its extra row source costs
   // the video-only kernel's gather warps issue slots even where it never runs.
-  auto kernel = n_text > 0 ? attention_tc_kernel<true> : attention_tc_kernel<false>;
+  auto kernel = n_text > 0 ? attention_tc_kernel<true, false>
+                           : (tma ? attention_tc_kernel<false, true> : attention_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
   if (e != cudaSuccess) return e;
   const int grid = std::max(1, std::min(sm_count(), prm.num_units));
