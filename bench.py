@@ -32,10 +32,11 @@ METRIC = "window-attention TFLOP/s per step (regular + shifted layer, transition
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes (read + write) of one regular-layout attention launch of the
-# 24-head 720p workload: an ncu capture of the same grid with 8 heads measured
-# 884.9 MB, scaled x3 (each head's rows are disjoint, so traffic grows with the
-# head count).  Valid only for the kernel source it was measured on.
-MEASURED_TRAFFIC = {"kernel_sha1": "7783a15c4584c29b", "workload": "720p", "heads": 24, "bytes": 2.657e9}
+# 24-head 720p workload with canonical rows: an ncu capture of the same grid
+# with 8 heads measured 884.8 MB, scaled x3 (each head's rows are disjoint, so
+# traffic grows with the head count).  Valid only for the kernel source it was
+# measured on.
+MEASURED_TRAFFIC = {"kernel_sha1": "ca77542972b6275a", "workload": "720p", "heads": 24, "bytes": 2.654e9}
 
 
 def kernel_sha1():
