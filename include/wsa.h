@@ -341,6 +341,23 @@ wsa_status wsa_gather_rows(const void* x, int x_rows, const int* index, void* y,
                            int rows, int channels, wsa_dtype dtype, void* stream);
 
 /*
+ * wsa_debug_withhold_units -- test hook for the failure path of the
+ * tensor-core attention kernel.  The pages have no counterpart: their
+ * coordination waits are bounded and report typed failures ("Window-Aligned
+ * Sequence Parallelism (SeedVR2)" and the runtime pages' failure handling),
+ * and this hook lets a test make such a wait run out on a GPU without a
+ * fault.  The next `launches` launches of that kernel (wsa_attention with
+ * bf16, wsa_attention_text, wsa_attention_noalloc) hand out no work unit:
+ * every role of the kernel waits for a unit that never comes, each wait gives
+ * up after about one second, the kernel records the code of the first wait
+ * that gave up in the plan's error word and returns without writing any
+ * output, and wsa_plan_device_status then reports WSA_ERR_DEVICE_CHECK.
+ * launches <= 0 turns the hook off.  Process-wide; a test uses it with no
+ * other attention launch in flight.
+ */
+wsa_status wsa_debug_withhold_units(int launches);
+
+/*
  * Reads and clears the plan's device error word (synchronises the device).
  * *code = 0 when no kernel recorded an error; otherwise the code of the first
  * bounded wait that gave up, and the call returns WSA_ERR_DEVICE_CHECK.

@@ -63,6 +63,7 @@ def _load():
         "wsa_sp_local_rows": ([i] * 10 + [ip, i, ip], i),
         "wsa_sp_plan_a": ([i] * 11 + [ctypes.POINTER(ctypes.c_longlong), ip, i, ip, i, ip, ip, ip], i),
         "wsa_gather_rows": ([p, i, p, p, i, i, i, p], i),
+        "wsa_debug_withhold_units": ([i], i),
         "wsa_rope": ([p, p, p, p, p, i, i, i, i, i, i, f, p], i),
         "wsa_sp_plan_b": ([i] * 8 + [ip, i, ip] + [ctypes.POINTER(ctypes.c_longlong)] * 3
                           + [ctypes.POINTER(ctypes.c_double)], i),
@@ -304,6 +305,14 @@ def gather_rows(x, index, out=None, stream=None):
     _check(lib.wsa_gather_rows(_ptr(x), x.shape[0], _ptr(index), _ptr(out), rows, x.shape[1], _dtype_code(x),
                                _stream(stream)))
     return out
+
+
+def debug_withhold_units(launches):
+    """wsa_debug_withhold_units: the next `launches` tensor-core attention
+    launches hand out no work unit, so every wait of the kernel runs out and
+    the plan's error word records the code (a test hook for the failure
+    path); 0 turns it off."""
+    _check(lib.wsa_debug_withhold_units(int(launches)))
 
 
 def attention_noalloc(T, H, W, nt, nh, nw, layout, q, k, v, out, canonical=True, scale=0.0,

@@ -22,6 +22,11 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" {
 
+wsa_status wsa_debug_withhold_units(int launches) {
+  withhold_attention_units(launches);
+  return WSA_OK;
+}
+
 wsa_status wsa_attention(wsa_plan_t plan, const void* q, const void* k, const void* v, void* o,
                          int heads, int head_dim, wsa_dtype dtype, int in_order_canonical,
                          float softmax_scale, void* stream) {

@@ -43,6 +43,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -132,6 +133,7 @@ struct TcParams {
   long long row_stride;  // bytes between consecutive tokens (heads * 256)
   float c;               // softmax scale * log2(e)
   int o_v8;              // output rows 32-byte aligned: 256-bit stores
+  int withhold_units;    // failure-path test hook: hand out no work unit
   int* work;             // workspace words
 };
 
@@ -496,6 +498,9 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
 // ready (up to two units ahead) before the gather warps finish the current one.
 __device__ __forceinline__ void scheduler_role(const TcParams& prm, const Smem& sm) {
   int* err = prm.work + WS_ERROR;
+  // Test hook: with no unit published, every other role's first wait runs
+  // out and the kernel unwinds with nothing in flight.
+  if (prm.withhold_units) return;
   for (uint32_t unit_iter = 0;; ++unit_iter) {
     const int us = unit_iter & 1;
     if (!wait_bar(bar_at(sm, B_UNIT_EMPTY + us), ((unit_iter >> 1) & 1) ^ 1, err, E_SCHED_UNIT_EMPTY)) break;
@@ -590,9 +595,17 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
     mbar_arrive(bar_at(sm, B_UNIT_EMPTY + us));
     ++unit_iter;
   }
-  // Drain: every MMA issued so far must finish before TMEM is freed.
+  // Drain: every MMA issued so far must finish before TMEM is freed, also
+  // when another role has given up (MMAs depend on nothing but their
+  // operands, so this wait ends unless the tensor core itself has stopped).
   tc_commit(bar_at(sm, B_DRAIN));
-  wait_bar(bar_at(sm, B_DRAIN), 0, err, E_MMA_DRAIN);
+  const long long t0 = clock64();
+  while (!mbar_try(bar_at(sm, B_DRAIN), 0)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicCAS(err, 0, E_MMA_DRAIN);
+      break;
+    }
+  }
 }
 
 // 32 bytes in one store (the address must be 32-byte aligned).
@@ -958,11 +971,23 @@ cudaError_t encode_rows(CUtensorMap* map, const void* base, int rows, int heads)
 
 }  // namespace
 
+namespace {
+std::atomic<int> g_withhold_launches{0};
+}  // namespace
+
+void withhold_attention_units(int launches) { g_withhold_launches.store(launches < 0 ? 0 : launches); }
+
 cudaError_t launch_attention_tc(const wsa_plan_s& p, const void* q, const void* k, const void* v, void* o, int heads,
                                 bool canonical, float scale, cudaStream_t s, const void* qt, const void* kt,
                                 const void* vt, float* text_part, int n_text, const WorkItem* items, int n_items) {
   TcParams prm;
   std::memset(&prm, 0, sizeof(prm));
+  for (int n = g_withhold_launches.load(); n > 0;) {
+    if (g_withhold_launches.compare_exchange_weak(n, n - 1)) {
+      prm.withhold_units = 1;
+      break;
+    }
+  }
   // Packed rows without a text segment: full tiles by TMA.
   const bool tma = !canonical && n_text == 0;
   if (tma) {

@@ -99,6 +99,9 @@ cudaError_t launch_attention_tc(const wsa_plan_s& p, const void* q, const void* 
                                 int heads, bool canonical, float scale, cudaStream_t s, const void* qt,
                                 const void* kt, const void* vt, float* text_part, int n_text,
                                 const WorkItem* items, int n_items);
+// Failure-path test hook: the next `launches` tensor-core attention launches
+// hand out no work unit (wsa_debug_withhold_units).
+void withhold_attention_units(int launches);
 // Workspace of the text form: its work list, then W x n_text x heads x 128
 // fp32 partials.  *items_bytes (optional) receives the work-list part.
 size_t attention_text_workspace_bytes(const wsa_plan_s& p, int n_text, int heads, size_t* items_bytes);
