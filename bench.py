@@ -332,6 +332,13 @@ def run_ours(args):
         traffic = mt["bytes"]
         traffic_note = ("DRAM bytes of the regular-layout launch (ncu capture of the 8-head case scaled x3); "
                         f"algorithmic {4.0 * N * wl.channels * 2:.3e} B")
+    fp32 = wl.dtype == "fp32"
+    if fp32:
+        # The fp32 path runs on the CUDA cores (FFMA): 128 fp32 lanes per SM,
+        # 2 FLOP per FMA, at the SM clock sampled during the timed region.
+        sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = clk.get("sm_mhz") or 2070.0
+        alu_peak = sm_count * 128 * 2 * mhz * 1e6 / 1e12
     a_reg = attn[:, 0::2].mean()
     a_sft = attn[:, 1::2].mean() if L > 1 else float("nan")
     attn_ms = attn.mean()
@@ -368,8 +375,8 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": f"synthetic (seeded torch.randn, {dist_note}, bf16)",
+        "dtype": "f32" if fp32 else "bf16",
+        "data": f"synthetic (seeded torch.randn, {dist_note}, {'fp32' if fp32 else 'bf16'})",
         "config": {"workload": f"{wl.name}: T={wl.T},H={wl.H},W={wl.W} ({N} tokens), nt,nh,nw={wl.nt},{wl.nh},{wl.nw} "
                                f"-> wt,wh,ww={plans[0].wt},{plans[0].wh},{plans[0].ww}; {wl.heads} heads x {wl.head_dim}; "
                                f"{L} alternating layers ("
@@ -396,6 +403,16 @@ def run_ours(args):
             "peak_source": f"{peak_kind} bf16 burst",
             "traffic": traffic,
             "traffic_note": traffic_note,
+        } if not fp32 else {
+            "bound": "alu",
+            "kernel": "attention_fp32_kernel",
+            "achieved": round(achieved, 4),
+            "peak": round(alu_peak, 2),
+            "unit": "TFLOP/s",
+            "frac": round(achieved / alu_peak, 5),
+            "peak_source": "derived: SMs x 128 fp32 lanes x 2 FLOP x sampled SM clock",
+            "traffic": None,
+            "traffic_note": "launch-bound parity workload; no ncu capture",
         },
         "e2e": e2e,
         "gpu_launches": (((2 if n_text else 1) + (0 if not use_rope else 2 if n_text else 1)) * L + L - 1)
@@ -459,6 +476,7 @@ def run_plan_a(args):
     torch.cuda.synchronize()
     clocks = ClockSampler(0)
     clocks.start()
+    time.sleep(0.3)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
