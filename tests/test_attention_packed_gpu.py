@@ -116,3 +116,40 @@ def test_neighbour_rows_never_enter_a_tile(wsa):
     keep[lo:hi] = False
     assert bool(torch.isfinite(o2[keep]).all())
     assert torch.equal(o2[keep], o_ref[keep])
+
+
+@pytest.mark.parametrize("heads", [1, 5])
+def test_packed_head_counts(wsa, heads):
+    # The tile maps' row stride is heads x 256 bytes: one head (rows back to
+    # back) and an odd count; whole-tile windows so that every tile is a TMA tile.
+    w = wsa_inputs.custom(8, 44, 76, 1, 4, 4, heads=heads, head_dim=128, name=f"whole-tiles-{heads}h")
+    g = _grid(w)
+    p = wsa.Plan(*g, 0)
+    op = oracle.make_plan(*g, 0)
+    q, k, v = wsa_inputs.qkv(w, device="cuda")
+    ids = torch.from_numpy(op.ids.astype(np.int64)).cuda()
+    o_can = wsa.attention(p, q, k, v)
+    o_pk = wsa.attention(p, _packed(q, ids), _packed(k, ids), _packed(v, ids), canonical=False)
+    assert p.device_status() == 0
+    assert torch.equal(o_pk, o_can[ids])
+    qn, kn, vn = (t.float().cpu().numpy() for t in (q, k, v))
+    on = o_pk.float().cpu().numpy()
+    for win in (0, op.num_windows - 1):
+        n = int(op.offsets[win + 1] - op.offsets[win])
+        ref = oracle.window_attention_rows(qn, kn, vn, op, win, heads - 1, np.arange(n))
+        assert_bf16_close(on[op.offsets[win]:op.offsets[win + 1], heads - 1, :], ref, f"{heads} heads win {win}")
+
+
+def test_single_full_tile_window(wsa):
+    # A grid whose one window is exactly one 128-row tile: Q, K and V all by TMA.
+    w = wsa_inputs.custom(2, 8, 8, 1, 1, 1, heads=2, head_dim=128, name="one-tile")
+    g = _grid(w)
+    p = wsa.Plan(*g, 0)
+    assert p.num_windows == 1 and p.num_tokens == 128
+    op = oracle.make_plan(*g, 0)
+    q, k, v = wsa_inputs.qkv(w, device="cuda")
+    ids = torch.from_numpy(op.ids.astype(np.int64)).cuda()
+    o_pk = wsa.attention(p, _packed(q, ids), _packed(k, ids), _packed(v, ids), canonical=False)
+    assert p.device_status() == 0
+    ref = oracle.window_attention(to64(q), to64(k), to64(v), op)[op.ids]
+    assert_bf16_close(to64(o_pk), ref, "one full tile")
