@@ -186,3 +186,61 @@ def test_argument_errors(wsa):
     with pytest.raises(wsa.WsaError):
         wsa.attention(p, x[:-1].contiguous(), x[:-1].contiguous(), x[:-1].contiguous())
     assert p.device_status() == 0
+
+
+@pytest.mark.parametrize("scale", [0.02, 0.3])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_explicit_softmax_scale(wsa, scale, dtype):
+    # softmax_scale > 0 replaces 1/sqrt(d).  0.3 is about 3.4x the default for
+    # d = 128: peaked rows whose running max jumps, so the lazy rescale of O runs.
+    if dtype == "bf16":
+        w = MID
+    else:
+        w = wsa_inputs.custom(5, 10, 12, 2, 4, 4, heads=2, head_dim=128, dtype="fp32", name="fp32-128")
+    p = wsa.Plan(*_grid(w), 1)
+    q, k, v = wsa_inputs.qkv(w)
+    o = wsa.attention(p, q.cuda(), k.cuda(), v.cuda(), scale=scale)
+    assert p.device_status() == 0
+    ref = oracle.window_attention(to64(q), to64(k), to64(v), oracle.make_plan(*_grid(w), 1), scale=scale)
+    if dtype == "bf16":
+        assert_bf16_close(to64(o), ref, f"bf16 scale {scale}")
+    else:
+        assert_fp32_close(to64(o), ref, f"fp32 scale {scale}")
+
+
+@pytest.mark.parametrize("canonical", [True, False], ids=["canonical", "packed"])
+def test_lazy_rescale_path(wsa, canonical):
+    # Keys after the first 128 packed rows of every window are scaled x8, so
+    # the row maxima of later key tiles exceed the first tile's by far more
+    # than the lazy threshold (about 30 against 24 in log2 units): most rows
+    # rescale O in TMEM at least once.
+    w = MID
+    g = _grid(w)
+    p = wsa.Plan(*g, 0)
+    op = oracle.make_plan(*g, 0)
+    q, k, v = wsa_inputs.qkv(w)
+    gain = torch.ones(w.num_tokens)
+    for win in range(op.num_windows):
+        rows = op.ids[op.offsets[win] + 128:op.offsets[win + 1]].astype(np.int64)
+        gain[torch.from_numpy(rows)] = 8.0
+    k = (k.float() * gain[:, None, None]).to(k.dtype)
+    # the case this test is for: most rows' max (log2 domain) grows by more than 24 after the first key tile
+    c = np.log2(np.e) / np.sqrt(128.0)
+    grown = total = 0
+    for win in range(op.num_windows):
+        rows = op.ids[op.offsets[win]:op.offsets[win + 1]].astype(np.int64)
+        s = to64(q[rows, 0]) @ to64(k[rows, 0]).T * c
+        grown += int(np.sum(s.max(axis=1) - s[:, :128].max(axis=1) > 24))
+        total += len(rows)
+    assert grown > total // 2
+    ref = oracle.window_attention(to64(q), to64(k), to64(v), op)
+    ids = torch.from_numpy(op.ids.astype(np.int64))
+    if canonical:
+        o = wsa.attention(p, q.cuda(), k.cuda(), v.cuda())
+        got = to64(o)
+    else:
+        o = wsa.attention(p, q[ids].contiguous().cuda(), k[ids].contiguous().cuda(), v[ids].contiguous().cuda(),
+                          canonical=False)
+        got = to64(o)[np.argsort(op.ids)]
+    assert p.device_status() == 0
+    assert_bf16_close(got, ref, f"lazy rescale ({'canonical' if canonical else 'packed'})")
