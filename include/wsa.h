@@ -184,9 +184,9 @@ wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src,
  * this is a deployment convenience of this library.
  *
  * Some callers cannot call cudaMalloc: their device memory is owned by
- * another framework's pool, their serving loop must not take the device-wide
- * synchronisation that cudaMalloc/cudaFree imply, or they run while a stream
- * is being captured.  They cannot create a plan, so this call takes the grid
+ * another framework's pool, or their serving loop must not take the
+ * device-wide synchronisation that cudaMalloc/cudaFree imply.  They cannot
+ * create a plan, so this call takes the grid
  * (T, H, W, nt, nh, nw, layout, max_temporal as in wsa_plan_create) directly
  * and builds the plan tables itself in a fixed device array inside the
  * library, then runs the same tensor-core attention kernel.  It allocates no

@@ -12,7 +12,7 @@ layouts":
   (max(.., 0) / min(.., size)) -- it is not a cyclic roll;
 * windows are enumerated with w outermost and t innermost.
 
-Readings where the note is silent (each one listed in the design doc):
+Readings where the note is silent:
 
 * ``round`` is Python's round-half-to-even on the fp64 product ``H * scale``
   (the note's pseudocode is Python).

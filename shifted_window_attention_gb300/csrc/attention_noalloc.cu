@@ -3,12 +3,11 @@
 //
 // Who needs it: code that runs where cudaMalloc is not an option -- a host
 // application whose device memory is entirely owned by another framework's
-// pool, a latency-critical serving loop that must not take the implicit
-// device synchronisation of cudaMalloc/cudaFree, or code that runs while a
-// stream is being captured, where allocation calls are not allowed.  Those
-// callers cannot create a plan (wsa_plan_create allocates the plan's tables),
-// so this entry point takes the grid and layout directly and keeps everything
-// the kernels need beyond the caller's tensors -- window offsets and boxes,
+// pool, or a latency-critical serving loop that must not take the implicit
+// device synchronisation of cudaMalloc/cudaFree.  Those callers cannot create
+// a plan (wsa_plan_create allocates the plan's tables), so this entry point
+// takes the grid and layout directly and keeps everything the kernels need
+// beyond the caller's tensors -- window offsets and boxes,
 // the ids/pos tables, the work list and the scheduler words -- in one
 // file-scope device array of fixed size.
 //

@@ -1,9 +1,9 @@
 """The allocation-free attention entry point, wsa_attention_noalloc.
 
 It serves callers that cannot call cudaMalloc -- device memory owned by
-another framework's pool, serving loops that must not take the device-wide
-synchronisation of cudaMalloc/cudaFree, code running under stream capture --
-and therefore cannot create a plan.  Its output must agree with the
+another framework's pool, or serving loops that must not take the
+device-wide synchronisation of cudaMalloc/cudaFree -- and therefore cannot
+create a plan.  Its output must agree with the
 plan-based wsa_attention within the bf16 tolerance the other tests use, on
 consecutive calls that reuse the library's fixed scratch array.
 
