@@ -134,6 +134,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def workload_config(wl, wsize, windows, packed=False, n_text=0, rope=-1, ws=1):
+    """The bench line's `config`: the workload, named by what it is (grid,
+    window sizes, heads, layers and what each step runs)."""
+    N, C, L = wl.num_tokens, wl.channels, wl.layers
+    desc = (f"{wl.name}: T={wl.T},H={wl.H},W={wl.W} ({N} tokens), nt,nh,nw={wl.nt},{wl.nh},{wl.nw} "
+            f"-> wt,wh,ww={wsize[0]},{wsize[1]},{wsize[2]}; {wl.heads} heads x {wl.head_dim}; "
+            f"{L} alternating layers ("
+            + ("attention on rows in plan-packed order, full tiles by TMA" if packed
+               else "attention gathers/scatters through ids")
+            + f") with {L - 1} transitions of [N,{C}]"
+            + (f"; segments [window, {n_text} text tokens], text mean over windows" if n_text else "")
+            + (f"; window-local 3D RoPE of Q/K (text_len {rope}) before each attention" if rope >= 0 else ""))
+    return {"workload": desc, "tokens": N, "heads": wl.heads, "head_dim": wl.head_dim, "layers": L,
+            "text_tokens": n_text, "windows": list(windows),
+            "l2": "inputs larger than L2 (Q/K/V >= 155 MB each); no flush",
+            "parallelism": "replicas" if ws > 1 else "single"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -377,20 +395,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32" if fp32 else "bf16",
         "data": f"synthetic (seeded torch.randn, {dist_note}, {'fp32' if fp32 else 'bf16'})",
-        "config": {"workload": f"{wl.name}: T={wl.T},H={wl.H},W={wl.W} ({N} tokens), nt,nh,nw={wl.nt},{wl.nh},{wl.nw} "
-                               f"-> wt,wh,ww={plans[0].wt},{plans[0].wh},{plans[0].ww}; {wl.heads} heads x {wl.head_dim}; "
-                               f"{L} alternating layers ("
-                               + ("attention on rows in plan-packed order, full tiles by TMA" if args.packed
-                                  else "attention gathers/scatters through ids")
-                               + f") with "
-                               f"{L - 1} transitions of [N,{C}]"
-                               + (f"; segments [window, {n_text} text tokens], text mean over windows" if n_text else "")
-                               + (f"; window-local 3D RoPE of Q/K (text_len {args.rope}) before each attention"
-                                  if use_rope else ""),
-                   "tokens": N, "heads": wl.heads, "head_dim": wl.head_dim, "layers": L, "text_tokens": n_text,
-                   "windows": [plans[0].num_windows, plans[1].num_windows],
-                   "l2": "inputs larger than L2 (Q/K/V >= 155 MB each); no flush",
-                   "parallelism": "replicas" if ws > 1 else "single"},
+        "config": workload_config(wl, (plans[0].wt, plans[0].wh, plans[0].ww),
+                                  [plans[0].num_windows, plans[1].num_windows], args.packed, n_text, args.rope, ws),
         "per_layer": per_layer,
         "roofline": {
             "bound": "tensor",
@@ -549,8 +555,10 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return None
+    import oracle
     import wsa_inputs
     wl = wsa_inputs.WORKLOADS[args.workload]
+    g = (wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw)
     inputs = cpu_inputs(wl)
     vals = []
     per = max(2.0, 90.0 / max(1, args.steps + args.warmup))
@@ -565,7 +573,8 @@ def run_reference(args):
         "metric": METRIC,
         "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name},
+        "config": workload_config(wl, oracle.window_size(wl.T, wl.H, wl.W, wl.nt, wl.nh, wl.nw),
+                                  [oracle.make_plan(*g, lay).num_windows for lay in (0, 1)], ws=ws),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"per step: {vals[0]['sample']}"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
