@@ -193,7 +193,8 @@ wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src,
  * device memory: no cudaMalloc, no cudaFree, no allocating library routine.
  *
  * q, k, v, o, heads, in_order_canonical, softmax_scale and stream as in
- * wsa_attention with dtype WSA_BF16 and head_dim 128 (fixed).
+ * wsa_attention with dtype WSA_BF16 and head_dim 128 (fixed); at most 65535
+ * heads (WSA_ERR_UNSUPPORTED beyond).
  *
  * Limits of the fixed array (about 4.4 MB, held by every GPU that loads the
  * library until the process exits): T*H*W <= 524288 tokens, at most 8192

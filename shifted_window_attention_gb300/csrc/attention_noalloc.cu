@@ -82,6 +82,7 @@ extern "C" wsa_status wsa_attention_noalloc(int T, int H, int W, int nt, int nh,
     return fail(WSA_ERR_INVALID_ARG, "layout must be WSA_REGULAR or WSA_SHIFTED");
   if (!q || !k || !v || !o) return fail(WSA_ERR_INVALID_ARG, "q, k, v and o must be non-null");
   if (heads <= 0) return fail(WSA_ERR_INVALID_ARG, "heads must be > 0");
+  if (heads > 65535) return fail(WSA_ERR_UNSUPPORTED, "at most 65535 heads");
   if (in_order_canonical != 0 && in_order_canonical != 1)
     return fail(WSA_ERR_INVALID_ARG, "in_order_canonical must be 0 or 1");
   if (!std::isfinite(softmax_scale)) return fail(WSA_ERR_INVALID_ARG, "softmax_scale is not finite");
