@@ -667,14 +667,17 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool firs
   tmem_ld128(tS, x);
   float mx;
   if (kFull) {
+    // columns 0-3 seed four chains, 4-123 take 15 rounds of 8, 124-127 close two chains
     float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
 #pragma unroll
-    for (int i = 4; i < 128; i += 8) {
+    for (int i = 4; i < 124; i += 8) {
       m0 = fmax3(m0, x[i], x[i + 1]);
       m1 = fmax3(m1, x[i + 2], x[i + 3]);
       m2 = fmax3(m2, x[i + 4], x[i + 5]);
       m3 = fmax3(m3, x[i + 6], x[i + 7]);
     }
+    m0 = fmax3(m0, x[124], x[125]);
+    m1 = fmax3(m1, x[126], x[127]);
     mx = fmax3(m0, m1, fmaxf(m2, m3));
   } else {
     mx = -INFINITY;
