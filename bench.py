@@ -29,6 +29,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "window-attention TFLOP/s per step (regular + shifted layer, transition included)"
+# Clock event reasons that invalidate a timed region (power capping does not).
+THROTTLE_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes (read + write) of one regular-layout attention launch of the
@@ -252,22 +254,31 @@ def run_ours(args):
     if any(p.device_status() for p in plans):
         raise RuntimeError("device error during warm-up")
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        step(i)
-    end.record(stream)
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
+    def timed_region():
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.3)
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        return start.elapsed_time(end), clocks.stop()
+
+    total_ms, clk = timed_region()
+    # A timed region that saw hardware or thermal slowdown is measured once more
+    # (every rank together); the second measurement is the one reported.
+    slow = float(bool(THROTTLE_REASONS & set(clk["reasons"])))
+    if max_over_ranks(slow, dist if ws > 1 else None, dev) > 0:
+        first = clk["reasons"]
+        total_ms, clk = timed_region()
+        clk["remeasured_after"] = first
     attn = np.array([[e[4 * l + 1].elapsed_time(e[4 * l + 2]) for l in range(L)] for e in ev])  # [steps, L]
     trans = np.array([[e[4 * l + 2].elapsed_time(e[4 * l + 3]) for l in range(L - 1)] for e in ev])
     rope_t = np.array([[e[4 * l].elapsed_time(e[4 * l + 1]) for l in range(L)] for e in ev])
@@ -297,7 +308,7 @@ def run_ours(args):
         in_ready = [torch.cuda.Event() for _ in range(2)]
         comp_done = [torch.cuda.Event() for _ in range(2)]
         out_done = [torch.cuda.Event() for _ in range(2)]
-        e2e_steps = max(2, min(args.steps, 10))
+        e2e_steps = max(2, args.steps)
 
         def e2e_run(n):
             for i in range(n):
@@ -480,17 +491,23 @@ def run_plan_a(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    clocks = ClockSampler(0)
-    clocks.start()
-    time.sleep(0.3)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    ms = t0.elapsed_time(t1) / args.steps
+    def timed_region():
+        clocks = ClockSampler(0)
+        clocks.start()
+        time.sleep(0.3)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / args.steps, clocks.stop()
+
+    ms, clk = timed_region()
+    if THROTTLE_REASONS & set(clk["reasons"]):
+        first = clk["reasons"]
+        ms, clk = timed_region()
+        clk["remeasured_after"] = first
     step_bytes = 2 * (2 * (2.0 * N * C * x.element_size()) + 2 * 4.0 * N)
     gbs = step_bytes / (ms * 1e-3) / 1e9
     peaks, peak_kind = load_peaks()
