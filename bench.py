@@ -28,7 +28,10 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "window-attention TFLOP/s per step (regular + shifted layer, transition included)"
+# The headline metric.  `value` is the attention FLOPs of all layers of a step
+# divided by the step time (attention layers plus the transitions between
+# them); tokens/s per layer and the fraction of tensor peak ride beside it.
+METRIC = "window-attention TFLOP/s & tokens/s per layer (bf16, 1\u00d7GB300); % tensor peak"
 # Clock event reasons that invalidate a timed region (power capping does not).
 THROTTLE_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -397,6 +400,7 @@ def run_ours(args):
         "metric": METRIC,
         "value": round(whole_job_tflops(fl_step, ms_step, ws), 2),
         "unit": "TFLOP/s",
+        "tokens_per_s": round(N * L * ws / (ms_step * 1e-3)),
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
