@@ -19,6 +19,13 @@
  *   wsa_last_error() returns (per host thread).
  * - Non-finite inputs are not validated: they propagate as IEEE arithmetic
  *   does.
+ * - Two builds export this same ABI.  libwsa.so is the product build.
+ *   libwsa_checked.so (compiled with -DWSA_BOUNDS_CHECK) also range-checks on
+ *   the device every row index it reads from a plan table before the index
+ *   addresses memory: an out-of-range index skips its access (the row reads as
+ *   zeros or is not written) and is reported by wsa_plan_device_status.  The
+ *   checked build stands in for a memory checker; its results on valid
+ *   tables are bit-identical to the product build's.
  */
 #ifndef WSA_H_
 #define WSA_H_
@@ -46,6 +53,9 @@ typedef enum { WSA_REGULAR = 0, WSA_SHIFTED = 1 } wsa_layout;
 
 /* Library ABI version (major*100 + minor). */
 int wsa_version(void);
+
+/* 1 in the bounds-checked build (libwsa_checked.so), 0 in libwsa.so. */
+int wsa_bounds_checked(void);
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* wsa_last_error(void);
@@ -359,9 +369,21 @@ wsa_status wsa_gather_rows(const void* x, int x_rows, const int* index, void* y,
 wsa_status wsa_debug_withhold_units(int launches);
 
 /*
- * Reads and clears the plan's device error word (synchronises the device).
+ * wsa_debug_fail_allocations -- test hook for the allocation failure path.
+ * The pages have no counterpart: their runtimes classify failures into typed
+ * errors, and this hook lets a test see this library's out-of-memory error
+ * without exhausting a GPU.  The next `count` device allocations of
+ * wsa_plan_create fail: the call returns WSA_ERR_OOM with a message naming
+ * the hook and creates nothing.  count <= 0 turns the hook off.  Process-wide.
+ */
+wsa_status wsa_debug_fail_allocations(int count);
+
+/*
+ * Reads and clears the plan's device error words (synchronises the device).
  * *code = 0 when no kernel recorded an error; otherwise the code of the first
- * bounded wait that gave up, and the call returns WSA_ERR_DEVICE_CHECK.
+ * bounded wait that gave up or, in the bounds-checked build, 0x401 when a
+ * kernel met a row index out of range in this plan's tables, and the call
+ * returns WSA_ERR_DEVICE_CHECK.
  */
 wsa_status wsa_plan_device_status(wsa_plan_t plan, int* code);
 

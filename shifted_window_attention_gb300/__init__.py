@@ -14,6 +14,8 @@ import os
 import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libwsa.so")
+# The same ABI built with device-side range checks of every plan-table index.
+_CHECKED_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libwsa_checked.so")
 
 REGULAR = 0
 SHIFTED = 1
@@ -38,14 +40,16 @@ class WsaError(RuntimeError):
         self.name = _STATUS.get(status, str(status))
 
 
-def _load():
-    if not os.path.exists(_LIB_PATH):
-        raise ImportError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build()")
-    lib = ctypes.CDLL(_LIB_PATH)
+def _load(path=_LIB_PATH):
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
     i, p, f = ctypes.c_int, ctypes.c_void_p, ctypes.c_float
     ip = ctypes.POINTER(ctypes.c_int)
     sigs = {
         "wsa_version": ([], i),
+        "wsa_bounds_checked": ([], i),
+        "wsa_debug_fail_allocations": ([i], i),
         "wsa_last_error": ([], ctypes.c_char_p),
         "wsa_window_size": ([i] * 7 + [ip] * 3, i),
         "wsa_layout_windows": ([i] * 8 + [ip, i, ip], i),
@@ -77,6 +81,18 @@ def _load():
 
 
 lib = _load()
+_checked = None
+
+
+def checked_library():
+    """The bounds-checked build (libwsa_checked.so) as a ctypes library with
+    the same signatures as `lib`: every plan-table row index is range-checked
+    on the device, and an index out of range is reported by
+    wsa_plan_device_status instead of addressing memory."""
+    global _checked
+    if _checked is None:
+        _checked = _load(_CHECKED_LIB_PATH)
+    return _checked
 
 
 def _check(status):

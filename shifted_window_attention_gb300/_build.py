@@ -1,5 +1,7 @@
-"""Builds libwsa.so in-tree: every CUDA source compiled for sm_103a with nvcc,
-in parallel, then linked into one shared library next to this file."""
+"""Builds the library in-tree: every CUDA source compiled for sm_103a with
+nvcc, in parallel, then linked into shared libraries next to this file:
+libwsa.so (the product build) and libwsa_checked.so (the same sources with
+-DWSA_BOUNDS_CHECK: every plan-table row index range-checked on the device)."""
 
 import concurrent.futures as cf
 import os
@@ -12,6 +14,10 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(REPO_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libwsa.so")
+CHECKED_LIB_PATH = os.path.join(PKG_DIR, "libwsa_checked.so")
+# (library, build folder, extra nvcc flags)
+VARIANTS = [(LIB_PATH, BUILD_DIR, []),
+            (CHECKED_LIB_PATH, os.path.join(REPO_DIR, "_build", "checked"), ["-DWSA_BOUNDS_CHECK"])]
 
 SOURCES = ["plan.cu", "transition.cu", "attention_fp32.cu", "attention_tc.cu", "abi.cu",
            "attention_noalloc.cu", "sp.cu", "rope.cu"]
@@ -36,10 +42,10 @@ def _deps():
     return files
 
 
-def _up_to_date():
-    if not os.path.exists(LIB_PATH):
+def _up_to_date(lib):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
@@ -51,25 +57,29 @@ def _run(cmd):
 
 
 def build(force=False, verbose=False, ptxas_verbose=False):
-    """Compile every source for sm_103a and link libwsa.so; returns its path."""
-    if not force and _up_to_date():
+    """Compile every source for sm_103a and link both libraries; returns the
+    product library's path."""
+    todo = [v for v in VARIANTS if force or not _up_to_date(v[0])]
+    if not todo:
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
     jobs = []
-    for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        jobs.append((obj, [nvcc, "-c", *ARCH, *FLAGS, *extra, "-I", INCLUDE, "-I", CSRC,
-                           os.path.join(CSRC, src), "-o", obj]))
+    for lib, bdir, defs in todo:
+        os.makedirs(bdir, exist_ok=True)
+        for src in SOURCES:
+            obj = os.path.join(bdir, src.replace(".cu", ".o"))
+            jobs.append((lib, obj, [nvcc, "-c", *ARCH, *FLAGS, *defs, *extra, "-I", INCLUDE, "-I", CSRC,
+                                    os.path.join(CSRC, src), "-o", obj]))
     with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
-        outs = list(ex.map(lambda j: _run(j[1]), jobs))
+        outs = list(ex.map(lambda j: _run(j[2]), jobs))
     if verbose or ptxas_verbose:
-        for (obj, _), out in zip(jobs, outs):
-            print(f"== {os.path.basename(obj)}\n{out}")
-    tmp = LIB_PATH + ".tmp"
-    _run([nvcc, "-shared", *ARCH, "-o", tmp] + [o for o, _ in jobs])
-    os.replace(tmp, LIB_PATH)
+        for (_, obj, _), out in zip(jobs, outs):
+            print(f"== {obj}\n{out}")
+    for lib, _, _ in todo:
+        tmp = lib + ".tmp"
+        _run([nvcc, "-shared", *ARCH, "-o", tmp] + [o for l, o, _ in jobs if l == lib])
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(kRows)
 attention_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                       const float* __restrict__ v, float* __restrict__ o,
                       const int* __restrict__ row_map, const int* __restrict__ offsets,
-                      const WorkItem* __restrict__ items, int heads, float scale) {
+                      const WorkItem* __restrict__ items, int heads, float scale, int n_tokens,
+                      int* __restrict__ bounds) {
   extern __shared__ float smem[];
   float* q_s = smem;                       // [kRows][D + 1] (padded: conflict-free row reads)
   float* k_s = q_s + kRows * (D + 1);      // [kKv][D]
@@ -42,11 +43,21 @@ attention_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   const int n = offsets[it.window + 1] - off;
   const int tid = threadIdx.x;
   const size_t stride = static_cast<size_t>(heads) * D;
-  auto token = [&](int r) -> long long { return row_map ? row_map[off + r] : off + r; };
+  // Token of window row r; -1 (bounds-checked builds) when the table entry is
+  // out of range: the row then reads as zeros and is not written.
+  auto token = [&](int r) -> long long {
+    const long long t = row_map ? row_map[off + r] : off + r;
+    if (kBoundsCheck && static_cast<unsigned long long>(t) >= static_cast<unsigned long long>(n_tokens)) {
+      atomicCAS(bounds, 0, kErrBounds);
+      return -1;
+    }
+    return t;
+  };
 
   const int qr = it.q_start + tid;
-  const bool q_valid = qr < n;
-  const long long q_tok = q_valid ? token(qr) : 0;
+  long long q_tok = qr < n ? token(qr) : -1;
+  const bool q_valid = q_tok >= 0;
+  if (!q_valid) q_tok = 0;
   for (int c = 0; c < D; ++c)
     q_s[tid * (D + 1) + c] = q_valid ? q[q_tok * stride + head * D + c] : 0.f;
 
@@ -60,13 +71,17 @@ attention_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     __syncthreads();  // previous tile fully consumed
     if (tid < kv_n) {
       const long long t = token(kv0 + tid);
-      const float4* ks = reinterpret_cast<const float4*>(k + t * stride + head * D);
-      const float4* vs = reinterpret_cast<const float4*>(v + t * stride + head * D);
       float4* kd = reinterpret_cast<float4*>(k_s + tid * D);
       float4* vd = reinterpret_cast<float4*>(v_s + tid * D);
-      for (int c = 0; c < D / 4; ++c) {
-        kd[c] = ks[c];
-        vd[c] = vs[c];
+      if (t >= 0) {
+        const float4* ks = reinterpret_cast<const float4*>(k + t * stride + head * D);
+        const float4* vs = reinterpret_cast<const float4*>(v + t * stride + head * D);
+        for (int c = 0; c < D / 4; ++c) {
+          kd[c] = ks[c];
+          vd[c] = vs[c];
+        }
+      } else {
+        for (int c = 0; c < D / 4; ++c) kd[c] = vd[c] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
     __syncthreads();
@@ -110,7 +125,8 @@ cudaError_t launch(const wsa_plan_s& p, const float* q, const float* k, const fl
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_simt_items, heads);
   attention_fp32_kernel<D><<<grid, kRows, smem, s>>>(q, k, v, o, canonical ? p.d_ids : nullptr,
-                                                     p.d_offsets, p.d_simt_items, heads, scale);
+                                                     p.d_offsets, p.d_simt_items, heads, scale, p.num_tokens,
+                                                     p.d_work + WS_BOUNDS);
   return cudaGetLastError();
 }
 

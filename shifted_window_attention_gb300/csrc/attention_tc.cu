@@ -119,6 +119,7 @@ struct TcParams {
   const WorkItem* items;
   int num_units;
   int heads;
+  int n_tokens;          // rows of q, k, v, o (bound of every ids entry)
   // Text segment (n_text = 0: video only).  Window w's attention runs over the
   // segment [its n_w video rows, the n_text text rows]; text query rows write
   // fp32 partials T_w / W to text_part[w][t][head][128].  The segment is tiled
@@ -387,7 +388,14 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
       ids[h] = -1;
       if (!kText || j < nvt) {
         const int myrow = j * kTile + lr;
-        if (myrow < nv) ids[h] = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+        if (myrow < nv) {
+          int id = prm.row_map ? __ldg(prm.row_map + off + myrow) : off + myrow;
+          if (kBoundsCheck && static_cast<unsigned>(id) >= static_cast<unsigned>(prm.n_tokens)) {
+            atomicCAS(prm.work + WS_BOUNDS, 0, kErrBounds);
+            id = -1;  // read as zeros
+          }
+          ids[h] = id;
+        }
       } else {
         const int tr = (j - nvt) * kTile + lr;
         if (tr < prm.n_text) ids[h] = tr;
@@ -782,10 +790,15 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
       const float inv = 1.f / ((la.x + la.y) + (lb.x + lb.y));
       const bool vtile = !kText || qtile < nvt;
       const int qr = (vtile ? qtile : qtile - nvt) * kTile + rq;  // row of the video or the text part
-      const bool valid = vtile && qr < nv;                          // a video row of this window
+      bool valid = vtile && qr < nv;                                // a video row of this window
       const bool text = kText && !vtile && qr < prm.n_text;         // a text row: partial T_w / W
       long long tok = 0;
       if (valid) tok = prm.row_map ? __ldg(prm.row_map + off + qr) : off + qr;
+      if (kBoundsCheck && valid && static_cast<unsigned long long>(tok) >= static_cast<unsigned long long>(prm.n_tokens)) {
+        atomicCAS(prm.work + WS_BOUNDS, 0, kErrBounds);
+        valid = false;  // not written
+        tok = 0;
+      }
       float* tdst = nullptr;
       if (text) {
         const long long window = static_cast<unsigned>(info.w) >> 16;
@@ -1047,6 +1060,7 @@ cudaError_t launch_attention_tc(const wsa_plan_s& p, const void* q, const void* 
   prm.n_text = n_text;
   prm.inv_windows = 1.0f / static_cast<float>(p.num_windows);
   prm.heads = heads;
+  prm.n_tokens = p.num_tokens;
   prm.row_stride = static_cast<long long>(heads) * kD * 2;
   prm.c = scale * 1.4426950408889634f;
   prm.o_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 && (prm.row_stride & 31) == 0;

@@ -10,6 +10,7 @@
 // convention (prefix sums from 0).
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -183,6 +184,18 @@ cudaError_t launch_plan_tables(const wsa_plan_s& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+namespace {
+// Test hook: the next g_fail_allocations plan allocations fail as if the
+// device were out of memory (wsa_debug_fail_allocations).
+std::atomic<int> g_fail_allocations{0};
+
+bool take_forced_failure() {
+  for (int n = g_fail_allocations.load(); n > 0;)
+    if (g_fail_allocations.compare_exchange_weak(n, n - 1)) return true;
+  return false;
+}
+}  // namespace
+
 }  // namespace wsa
 
 using namespace wsa;
@@ -190,6 +203,13 @@ using namespace wsa;
 extern "C" {
 
 int wsa_version(void) { return 100; }
+
+int wsa_bounds_checked(void) { return kBoundsCheck ? 1 : 0; }
+
+wsa_status wsa_debug_fail_allocations(int count) {
+  g_fail_allocations.store(count < 0 ? 0 : count);
+  return WSA_OK;
+}
 
 const char* wsa_last_error(void) { return g_last_error.c_str(); }
 
@@ -261,6 +281,10 @@ wsa_status wsa_plan_create(int T, int H, int W, int nt, int nh, int nw, wsa_layo
   size_t total = align_up(off_work + WS_WORDS * sizeof(int), a);
 
   cudaError_t e = cudaGetDevice(&p->device);
+  if (e == cudaSuccess && take_forced_failure()) {
+    delete p;
+    return fail(WSA_ERR_OOM, "wsa_plan_create: device allocation failed (forced by wsa_debug_fail_allocations)");
+  }
   if (e == cudaSuccess) e = cudaMalloc(&p->d_block, total);
   if (e != cudaSuccess) {
     delete p;
@@ -335,15 +359,20 @@ wsa_status wsa_plan_device_status(wsa_plan_t plan, int* code) {
   if (!plan || !code) return fail(WSA_ERR_INVALID_ARG, "plan or code is null");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "wsa_plan_device_status: synchronize");
-  int word = 0;
-  e = cudaMemcpy(&word, plan->d_work + WS_ERROR, sizeof(int), cudaMemcpyDeviceToHost);
+  // WS_ERROR and WS_BOUNDS are adjacent words: read and clear both.
+  static_assert(WS_BOUNDS == WS_ERROR + 1, "error words must be adjacent");
+  int words[2] = {0, 0};
+  e = cudaMemcpy(words, plan->d_work + WS_ERROR, sizeof(words), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "wsa_plan_device_status: read");
-  *code = word;
-  if (word != 0) {
-    const int zero = 0;
-    e = cudaMemcpy(plan->d_work + WS_ERROR, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  *code = words[0] != 0 ? words[0] : words[1];
+  if (*code != 0) {
+    const int zero[2] = {0, 0};
+    e = cudaMemcpy(plan->d_work + WS_ERROR, zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "wsa_plan_device_status: clear");
-    return fail(WSA_ERR_DEVICE_CHECK, "a kernel recorded device error code " + std::to_string(word));
+    if (words[0] != 0)
+      return fail(WSA_ERR_DEVICE_CHECK, "a kernel recorded device error code " + std::to_string(words[0]));
+    return fail(WSA_ERR_DEVICE_CHECK, "a plan table held a row index out of range (device code " +
+                                          std::to_string(words[1]) + ", bounds-checked build)");
   }
   return WSA_OK;
 }

@@ -39,8 +39,22 @@ enum WorkspaceWord {
   WS_NEXT_UNIT = 0,   // dynamic scheduler: next unit to hand out
   WS_DONE_CTAS = 1,   // CTAs that finished (the last one resets both counters)
   WS_ERROR = 2,       // first error code recorded by a kernel (0 = none)
+  WS_BOUNDS = 3,      // bounds-checked builds: a table index was out of range
   WS_WORDS = 8
 };
+
+// Bounds-checked builds (compiled with -DWSA_BOUNDS_CHECK, libwsa_checked.so):
+// every row index read from a plan table is range-checked on the device
+// before it addresses memory.  An index out of range skips its access (the
+// row reads as zeros or is not written) and records kErrBounds in the plan's
+// WS_BOUNDS word, which wsa_plan_device_status reports; the kernel itself
+// runs to completion.
+#ifdef WSA_BOUNDS_CHECK
+constexpr bool kBoundsCheck = true;
+#else
+constexpr bool kBoundsCheck = false;
+#endif
+constexpr int kErrBounds = 0x401;
 
 // Query rows covered by one work item of each attention kernel.
 constexpr int kTcItemRows = 256;    // tensor-core kernel: two 128-row tiles

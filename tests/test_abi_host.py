@@ -35,10 +35,17 @@ def test_header_declares_the_boundary():
         assert name in syms
 
 
-def test_library_exports_every_declared_symbol(wsa):
-    lib = ctypes.CDLL(wsa._LIB_PATH)
+@pytest.mark.parametrize("which", ["product", "checked"])
+def test_library_exports_every_declared_symbol(wsa, which):
+    lib = ctypes.CDLL(wsa._LIB_PATH if which == "product" else wsa._CHECKED_LIB_PATH)
     missing = [s for s in declared_symbols() if not hasattr(lib, s)]
     assert missing == []
+
+
+def test_bounds_checked_flag(wsa):
+    # the product build runs no device range checks; the checked build does
+    assert wsa.lib.wsa_bounds_checked() == 0
+    assert wsa.checked_library().wsa_bounds_checked() == 1
 
 
 def test_version(wsa):
