@@ -119,6 +119,12 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        return self.summarize(out)
+
+    @staticmethod
+    def summarize(out):
+        """Median SM clock of the loaded samples, the maximum clock and the
+        clock event reasons seen active, from nvidia-smi's CSV lines."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():

@@ -58,3 +58,30 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch):
         steps = 1
         warmup = 0
     assert bench.run_reference(Args()) is None
+
+
+def test_clock_summary_reads_reasons_and_loaded_median():
+    lines = "\n".join([
+        "0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 1300.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 345, 2070, 120.0, 0x1, Not Active, Not Active, Not Active, Not Active",  # idle sample
+    ])
+    c = bench.ClockSampler.summarize(lines)
+    assert c["sm_max_mhz"] == 2070.0
+    assert c["sm_mhz"] == 2070.0  # median of the three loaded samples; the idle one is dropped
+    assert c["reasons"] == ["sw_power_cap"]
+    assert not (bench.THROTTLE_REASONS & set(c["reasons"]))  # power capping keeps the run
+    hot = bench.ClockSampler.summarize("0, 1500, 2070, 1400.0, 0x40, Not Active, Active, Not Active, Not Active")
+    assert bench.THROTTLE_REASONS & set(hot["reasons"]) == {"hw_thermal_slowdown"}  # measured again
+
+
+def test_workload_config_names_the_workload():
+    import wsa_inputs
+    wl = wsa_inputs.WORKLOADS["720p"]
+    c = bench.workload_config(wl, (6, 15, 27), [36, 64])
+    assert c["tokens"] == 75600 and c["heads"] == 24 and c["head_dim"] == 128 and c["windows"] == [36, 64]
+    assert c["workload"].startswith("720p: T=21,H=45,W=80 (75600 tokens)")
+    assert "wt,wh,ww=6,15,27" in c["workload"] and "gathers/scatters through ids" in c["workload"]
+    assert "plan-packed order" in bench.workload_config(wl, (6, 15, 27), [36, 64], packed=True)["workload"]
+    assert c["parallelism"] == "single" and bench.workload_config(wl, (6, 15, 27), [36, 64], ws=2)["parallelism"] == "replicas"
