@@ -158,6 +158,19 @@ def test_full_size_sampled(wsa, name, layout):
     _check_sampled(wsa, WORKLOADS[name], layout)
 
 
+@pytest.mark.parametrize("layout", [0, 1])
+def test_720p_every_window_and_head(wsa, layout):
+    # the headline workload compared in full: every output element of both
+    # layouts (36 / 64 windows x 24 heads) against the fp64 oracle
+    w = WORKLOADS["720p"]
+    p = wsa.Plan(*_grid(w), layout)
+    q, k, v = wsa_inputs.qkv(w, layer=0)
+    o = wsa.attention(p, q.cuda(), k.cuda(), v.cuda())
+    assert p.device_status() == 0
+    ref = oracle.window_attention(to64(q), to64(k), to64(v), oracle.make_plan(*_grid(w), layout))
+    assert_bf16_close(to64(o), ref, f"720p layout {layout}, all windows and heads")
+
+
 def test_32layer_schedule_sampled(wsa):
     # alternating layouts, fresh Q/K/V per layer; layers 0 and 1 plus a seeded
     # sample of later layers
