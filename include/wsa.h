@@ -184,6 +184,9 @@ wsa_status wsa_attention_text(wsa_plan_t plan, const void* q, const void* k,
  * x_src, x_dst: device, [N, channels] contiguous of `dtype`, must not
  * overlap.  src and dst may be the same plan (plain copy).  Plans of
  * different grids: WSA_ERR_MISMATCH.  Bit-exact (pure data movement).
+ * A table entry out of range at either level (possible only if a caller has
+ * written into the plan tables) skips its row, which is left unwritten; the
+ * bounds-checked build also reports it through wsa_plan_device_status(dst).
  */
 wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src,
                           void* x_dst, int channels, wsa_dtype dtype, void* stream);
