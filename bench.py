@@ -446,7 +446,7 @@ def run_ours(args):
                         * args.steps,
         "clocks": clk,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:  # the CPU baseline is an N = 1 figure
         q0, k0, v0 = sets[0]
         result["cpu_baseline"] = cpu_baseline(wl, tuple(t.float().cpu().numpy() for t in (q0, k0, v0)),
                                               seconds=args.cpu_seconds)
