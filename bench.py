@@ -38,10 +38,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) of one regular-layout attention launch of the
 # 24-head 720p workload with canonical rows: an ncu capture of the same grid
-# with 8 heads measured 884.9 MB, scaled x3 (each head's rows are disjoint, so
+# with 8 heads measured 885.3 MB, scaled x3 (each head's rows are disjoint, so
 # traffic grows with the head count).  Valid only for the kernel source it was
 # measured on.
-MEASURED_TRAFFIC = {"kernel_sha1": "c05cf23ad2db2ab7", "workload": "720p", "heads": 24, "bytes": 2.655e9}
+MEASURED_TRAFFIC = {"kernel_sha1": "66187d7c5da48c79", "workload": "720p", "heads": 24, "bytes": 2.656e9}
 
 
 def kernel_sha1():

@@ -75,6 +75,22 @@ def test_packed_order_matches_canonical(wsa):
     assert torch.equal(op.cpu(), o.cpu()[ids])
 
 
+def test_output_16_byte_aligned_only(wsa):
+    # an output that is 16- but not 32-byte aligned takes the 16-byte store
+    # path; it must write exactly what the 32-byte path writes
+    w = MID
+    p = wsa.Plan(*_grid(w), 1)
+    q, k, v = (t.cuda() for t in wsa_inputs.qkv(w, layer=5))
+    expect = wsa.attention(p, q, k, v)
+    buf = torch.full((q.numel() + 8,), float("nan"), dtype=q.dtype, device="cuda")
+    out = buf[8:].view(q.shape)  # 16 bytes past a 256-byte aligned base
+    assert out.data_ptr() % 32 == 16
+    wsa.attention(p, q, k, v, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, expect)
+    assert bool(torch.isnan(buf[:8]).all())
+
+
 def test_repeat_calls_identical(wsa):
     w = MID
     p, (q, k, v), o = _run(wsa, w, 0)
