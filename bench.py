@@ -163,6 +163,27 @@ def workload_config(wl, wsize, windows, packed=False, n_text=0, rope=-1, ws=1):
             "parallelism": "replicas" if ws > 1 else "single"}
 
 
+def host_link_gbs(host, device, stream):
+    """Pinned host <-> device copy bandwidth (GB/s, each direction alone, best
+    of three) measured right after the end-to-end leg: the host link is
+    shared with the other GPUs of the machine, and this says what it gave."""
+    import torch
+    out = {}
+    for name, dst, src in (("h2d", device, host), ("d2h", host, device)):
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                dst.copy_(src, non_blocking=True)
+                b.record(stream)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        out[name] = round(src.numel() * src.element_size() / (best * 1e-3) / 1e9, 1)
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -360,7 +381,8 @@ def run_ours(args):
         e2e = {"value": round(whole_job_tflops(fl_step, e2e_ms, ws), 2), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": e2e_steps,
-               "pipeline": "uploads, compute and downloads on three streams, two device buffer sets"}
+               "pipeline": "uploads, compute and downloads on three streams, two device buffer sets",
+               "host_link_gbs": host_link_gbs(host_in[0], dev_sets[0][0], s_in)}
 
     peaks, peak_kind = load_peaks()
     traffic, traffic_note = None, "no ncu capture for this kernel source / workload"
