@@ -1,9 +1,9 @@
 """The bounds-checked build (libwsa_checked.so) and the allocation-failure hook.
 
-Compute-sanitizer is not available on this machine, so the library ships a
-second build of the same sources in which every row index read from a plan
-table is range-checked on the device before it addresses memory.  These tests
-call it through the C ABI and check that:
+The library ships a second build of the same sources, a stand-in for a
+memory checker, in which every row index read from a plan table is
+range-checked on the device before it addresses memory.  These tests call it
+through the C ABI and check that:
 
 * on valid tables its results are bit-identical to the product build's, with
   a clean device status;
