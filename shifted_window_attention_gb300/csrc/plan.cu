@@ -150,7 +150,10 @@ namespace {
 __global__ void plan_tables_kernel(const int* __restrict__ offsets, const int* __restrict__ dims,
                                    int num_windows, int H, int W, int N, int* __restrict__ ids,
                                    int* __restrict__ pos) {
-  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < N; p += gridDim.x * blockDim.x) {
+  // 64-bit loop index: p + stride must not overflow for N close to 2^31
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long pp = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; pp < N; pp += stride) {
+    const int p = static_cast<int>(pp);
     int lo = 0, hi = num_windows - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
