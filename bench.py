@@ -209,17 +209,21 @@ def run_ours(args):
     torch.cuda.synchronize()
     plan_ms = (time.perf_counter() - t0) * 1e3
 
-    # Layer schedule: layout of layer l is regular for even l, shifted for odd
-    # l; a transition of the hidden state [N, C] runs between consecutive
-    # layers (L - 1 of them).  Inputs: seeded Q/K/V per layer; schedules longer
-    # than 4 layers cycle 4 seeded input sets (the values do not change the work).
+    # Layer schedule: the layout each layer requires, as the model lists it
+    # (NaDiT alternates regular and shifted windows).  Before every layer after
+    # the first, ensure_layout(current, required) brings the hidden state
+    # [N, C] into that layer's packed order; the transitions are derived from
+    # this list, one wherever consecutive layers differ (L - 1 of them here).
+    # Inputs: seeded Q/K/V per layer; schedules longer than 4 layers cycle 4
+    # seeded input sets (the values do not change the work).
+    layer_layouts = [(wsa.REGULAR, wsa.SHIFTED)[l % 2] for l in range(L)]
     n_sets = min(L, 4)
     sets = [wsa_inputs.qkv(wl, layer=i, device=dev) for i in range(n_sets)]
     canonical = not args.packed
     if args.packed:
         # rows in the plan-packed order of each set's layout (untimed setup)
         for i in range(n_sets):
-            ids = plans[i % 2].tables()[2].long()
+            ids = plans[layer_layouts[i]].tables()[2].long()
             sets[i] = tuple(t[ids].contiguous() for t in sets[i])
     outs = [torch.empty_like(sets[i % n_sets][0]) for i in range(min(L, 2))]
     n_text = args.text
@@ -236,7 +240,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     flops = [attn_flops(p.tables()[0].cpu().numpy(), wl.heads, wl.head_dim, n_text) for p in plans]
-    fl_step = sum(flops[l % 2] for l in range(L))
+    fl_step = sum(flops[layer_layouts[l]] for l in range(L))
     trans_bytes = 2.0 * N * C * 2 + 2 * 4.0 * N  # read + write rows, two int32 table reads
 
     use_rope = args.rope >= 0
@@ -255,13 +259,16 @@ def run_ours(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
 
     def step(i=None):
+        """One pass over the layer list; returns the transitions it ran."""
         e = ev[i] if i is not None else None
+        h, spare, moves = hidden[0], hidden[1], 0
         for l in range(L):
+            p = plans[layer_layouts[l]]
             q, k, v = sets[l % n_sets]
             if e: e[4 * l].record(stream)
             if use_rope:
                 qr, kr = qk_rot[l % 2]
-                wsa.rope(plans[l % 2], q, k, q_out=qr, k_out=kr, text_len=args.rope)
+                wsa.rope(p, q, k, q_out=qr, k_out=kr, text_len=args.rope)
                 q, k = qr, kr
             if n_text:
                 qt, kt, vt = tsets[l % n_sets]
@@ -269,17 +276,21 @@ def run_ours(args):
                     qt, kt = wsa.rope_text(qt, kt, q_out=tqk_rot[l % 2][0], k_out=tqk_rot[l % 2][1])
             if e: e[4 * l + 1].record(stream)
             if n_text:
-                wsa.attention_text(plans[l % 2], q, k, v, qt, kt, vt, out=outs[l % 2],
+                wsa.attention_text(p, q, k, v, qt, kt, vt, out=outs[l % 2],
                                    out_txt=touts[l % 2], workspace=wspace[l % 2])
             else:
-                wsa.attention(plans[l % 2], q, k, v, out=outs[l % 2], canonical=canonical)
+                wsa.attention(p, q, k, v, out=outs[l % 2], canonical=canonical)
             if e: e[4 * l + 2].record(stream)
             if l + 1 < L:
-                wsa.transition(plans[l % 2], plans[(l + 1) % 2], hidden[l % 2], out=hidden[(l + 1) % 2])
+                # the hidden state enters the next layer's layout
+                x = wsa.ensure_layout(p, plans[layer_layouts[l + 1]], h, out=spare)
+                if x is not h:
+                    h, spare, moves = x, h, moves + 1
             if e: e[4 * l + 3].record(stream)
+        return moves
 
     for _ in range(args.warmup):
-        step()
+        transitions = step()
     torch.cuda.synchronize()
     if any(p.device_status() for p in plans):
         raise RuntimeError("device error during warm-up")
@@ -399,8 +410,9 @@ def run_ours(args):
         sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
         mhz = clk.get("sm_mhz") or 2070.0
         alu_peak = sm_count * 128 * 2 * mhz * 1e6 / 1e12
-    a_reg = attn[:, 0::2].mean()
-    a_sft = attn[:, 1::2].mean() if L > 1 else float("nan")
+    kinds = np.array(layer_layouts)
+    a_reg = attn[:, kinds == wsa.REGULAR].mean()
+    a_sft = attn[:, kinds == wsa.SHIFTED].mean() if (kinds == wsa.SHIFTED).any() else float("nan")
     attn_ms = attn.mean()
     fl_launch = fl_step / L
     achieved = fl_launch / (attn_ms * 1e-3) / 1e12
@@ -464,7 +476,7 @@ def run_ours(args):
             "traffic_note": "launch-bound parity workload; no ncu capture",
         },
         "e2e": e2e,
-        "gpu_launches": (((2 if n_text else 1) + (0 if not use_rope else 2 if n_text else 1)) * L + L - 1)
+        "gpu_launches": (((2 if n_text else 1) + (0 if not use_rope else 2 if n_text else 1)) * L + transitions)
                         * args.steps,
         "clocks": clk,
     }

@@ -93,14 +93,22 @@ wsa_status wsa_layout_windows(int T, int H, int W, int nt, int nh, int nw,
  * kernel writes ids[p] = canonical id (t*H + h)*W + w of packed position p
  * (windows in enumeration order, tokens row-major in (t, h, w) inside a
  * window -- "Window layouts") and pos[ids[p]] = p.
- * N = T*H*W must be < 2^31.  The plan allocates its tables with cudaMalloc
- * (synchronous); they are filled asynchronously on `stream`.
+ * N = T*H*W must be < 2^31.  The plan allocates its tables stream-ordered
+ * (cudaMallocAsync on `stream`, no device-wide synchronisation) and fills
+ * them asynchronously on `stream`; work on another stream must be ordered
+ * after that stream before it uses the plan.
  */
 wsa_status wsa_plan_create(int T, int H, int W, int nt, int nh, int nw,
                            wsa_layout layout, int max_temporal, void* stream,
                            wsa_plan_t* out);
 
-/* Frees the plan and its device tables (cudaFree: synchronises the device). */
+/*
+ * Frees the plan and its device tables.  The tables are released
+ * stream-ordered (cudaFreeAsync) on the stream of the plan's latest call --
+ * its creation or the last launch that used it -- which must still exist;
+ * work on other streams that uses the plan must be ordered before that
+ * stream's release.  Does not synchronise the device.
+ */
 wsa_status wsa_plan_destroy(wsa_plan_t plan);
 
 /* Sizes of a plan.  Any output pointer may be NULL. */
@@ -192,6 +200,26 @@ wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src,
                           void* x_dst, int channels, wsa_dtype dtype, void* stream);
 
 /*
+ * wsa_ensure_layout -- brings the activations into the layout a layer needs.
+ * "Window-Aligned Sequence Parallelism (SeedVR2)", section "Window layouts":
+ * the number of layout transitions follows the model's actual layer
+ * schedule; ensure_layout(current, required) derives each one before a layer
+ * instead of assuming that layer l uses layout l % 2.
+ *
+ * x: device, [N, channels] of `dtype`, rows in the packed order of
+ * `current`.  When `required` describes the same windows as `current` (same
+ * grid, same window size, same layout) the rows are already in the required
+ * order: nothing is launched and *moved = 0.  Otherwise the rows are
+ * rearranged into x_out exactly as wsa_transition(current, required, x,
+ * x_out, ...) does, and *moved = 1; the caller's activations then live in
+ * x_out.  x_out may be null only when no transition is needed (the call
+ * fails with WSA_ERR_INVALID_ARG otherwise).  Errors as wsa_transition.
+ */
+wsa_status wsa_ensure_layout(wsa_plan_t current, wsa_plan_t required, const void* x,
+                             void* x_out, int channels, wsa_dtype dtype, void* stream,
+                             int* moved);
+
+/*
  * wsa_attention_noalloc -- the bf16 window attention of wsa_attention for
  * callers that cannot allocate device memory.  The pages have no counterpart:
  * this is a deployment convenience of this library.
@@ -215,18 +243,32 @@ wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src,
  * returns WSA_ERR_UNSUPPORTED with a message naming the limit.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call reuses the same array and overwrites what the previous
- * call left there, so calls whose GPU work overlaps (other streams, other
- * host threads) race and must be ordered by the caller.  A device-side wait
- * that gives up is not reported by this call (use wsa_attention with a plan
- * and wsa_plan_device_status for that).
+ * device, with that device current) and keeps it for the life of the
+ * process; make that first call before any stream capture, and make no call
+ * after a reset of the device (cudaDeviceReset destroys the array).  Every
+ * call reuses the same array and overwrites what the previous call left
+ * there, so calls whose GPU work overlaps (other streams, other host
+ * threads) race and must be ordered by the caller.  A device-side wait that
+ * gives up records its code in the array instead of returning it:
+ * wsa_noalloc_device_status reads it, and the next call clears it.
  */
 wsa_status wsa_attention_noalloc(int T, int H, int W, int nt, int nh, int nw,
                                  wsa_layout layout, int max_temporal,
                                  const void* q, const void* k, const void* v,
                                  void* o, int heads, int in_order_canonical,
                                  float softmax_scale, void* stream);
+
+/*
+ * wsa_noalloc_device_status -- the device error words of the last
+ * wsa_attention_noalloc call on the current device (no counterpart in the
+ * pages, like the call it serves).  Synchronises the device, reads the error
+ * word a kernel of that call recorded in the fixed array (a bounded wait that
+ * gave up; in the bounds-checked build also an out-of-range table index),
+ * clears it, and returns WSA_ERR_DEVICE_CHECK with the code in *code, or
+ * WSA_OK with *code = 0.  The next wsa_attention_noalloc call clears the
+ * words itself, so read them before it.  Allocates no device memory.
+ */
+wsa_status wsa_noalloc_device_status(int* code);
 
 /*
  * wsa_rope -- window-local 3D rotary position embedding of Q and K.
@@ -310,14 +352,20 @@ wsa_status wsa_sp_local_rows(int T, int H, int W, int nt, int nh, int nw,
  *   *network_exchange_required: 1 if any row changes rank.  It is computed
  *     from the global matrix, so every rank gets the same value.  When it is
  *     0, the exchange is the local permutation x[send_index[recv_index[p]]].
- * Both index tables are int32 on the host; rows counts fit in int.
+ *   local_index [*n_recv] (may be NULL): that composed index,
+ *     local_index[p] = send_index[recv_index[p]], the one gather of the
+ *     local-permutation fast path.  Written only when
+ *     *network_exchange_required is 0 (then *n_send == *n_recv).
+ * Every index table is int32 on the host; row counts fit in int.  A capacity
+ * below the count it must hold is WSA_ERR_INVALID_ARG.
  */
 wsa_status wsa_sp_plan_a(int T, int H, int W, int nt, int nh, int nw,
                          wsa_layout src_layout, wsa_layout dst_layout,
                          int max_temporal, int ranks, int rank,
                          long long* counts, int* send_index, int send_capacity,
-                         int* recv_index, int recv_capacity, int* n_send,
-                         int* n_recv, int* network_exchange_required);
+                         int* recv_index, int recv_capacity, int* local_index,
+                         int local_capacity, int* n_send, int* n_recv,
+                         int* network_exchange_required);
 
 /*
  * wsa_sp_plan_b -- host only: the counts of a Plan B halo exchange for one
@@ -341,6 +389,47 @@ wsa_status wsa_sp_plan_b(int T, int H, int W, int nt, int nh, int nw,
                          int max_temporal, int ranks, int* window_rank,
                          int capacity, int* num_windows, long long* halo_in,
                          long long* halo_out, long long* tokens, double* work);
+
+/*
+ * wsa_sp_crossover -- host only: Plan A against Plan B for one regular +
+ * shifted layer pair, the crossover evaluation that the note leaves open
+ * ("Window-Aligned Sequence Parallelism (SeedVR2)", section "Limitations";
+ * Plan B read as in wsa_sp_plan_b).  Rows are hidden-state rows of
+ * `channels` elements of `bytes_per_elem` bytes.
+ *   plan_a_bytes: rows that change rank at the regular -> shifted and the
+ *     shifted -> regular boundary (off-diagonal counts of both matrices);
+ *   plan_a_max_rank_bytes: per boundary the busiest rank's rows sent or
+ *     received (whichever is larger), summed over the two boundaries; it
+ *     bounds the all-to-all time;
+ *   plan_b_bytes, plan_b_max_rank_bytes: the halo rows in plus their outputs
+ *     back (twice the halo counts), total and for the busiest rank;
+ *   plan_*_shifted_imbalance: the shifted layer's attention work (sum of
+ *     n_w^2) on the busiest rank over the mean, Plan A under its LPT owners,
+ *     Plan B under its computing ranks.
+ * With shifted_ms > 0, the measured one-GPU time of the shifted attention
+ * layer, each plan's busiest-rank attention time is estimated as shifted_ms
+ * times its share of the total sum of n_w^2 (plan_*_shifted_ms_max_rank), and
+ * crossover_link_gbs is the link bandwidth below which Plan B's smaller
+ * exchange outweighs its imbalance: the difference of the busiest ranks'
+ * bytes over the difference of their attention times.  Fields that do not
+ * apply (no shifted_ms, or Plan B never wins) are -1.
+ */
+typedef struct {
+  long long plan_a_bytes;
+  long long plan_a_max_rank_bytes;
+  long long plan_b_bytes;
+  long long plan_b_max_rank_bytes;
+  double plan_a_shifted_imbalance;
+  double plan_b_shifted_imbalance;
+  double plan_a_shifted_ms_max_rank;
+  double plan_b_shifted_ms_max_rank;
+  double crossover_link_gbs;
+} wsa_sp_crossover_t;
+
+wsa_status wsa_sp_crossover(int T, int H, int W, int nt, int nh, int nw,
+                            int max_temporal, int ranks, int channels,
+                            int bytes_per_elem, double shifted_ms,
+                            wsa_sp_crossover_t* out);
 
 /*
  * wsa_gather_rows -- y[i] = x[index[i]] for 0 <= i < rows: the pack
@@ -382,7 +471,10 @@ wsa_status wsa_debug_withhold_units(int launches);
 wsa_status wsa_debug_fail_allocations(int count);
 
 /*
- * Reads and clears the plan's device error words (synchronises the device).
+ * Reads and clears the plan's device error words.  Synchronises the stream
+ * of the plan's latest call (not the whole device): calls that use one plan
+ * are ordered on one stream, so every launch that can have recorded an
+ * error in it has finished.
  * *code = 0 when no kernel recorded an error; otherwise the code of the first
  * bounded wait that gave up or, in the bounds-checked build, 0x401 when a
  * kernel met a row index out of range in this plan's tables, and the call

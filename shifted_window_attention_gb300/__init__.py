@@ -59,13 +59,16 @@ def _load(path=_LIB_PATH):
         "wsa_plan_tables": ([p] + [ctypes.POINTER(p)] * 4, i),
         "wsa_attention": ([p, p, p, p, p, i, i, i, i, f, p], i),
         "wsa_transition": ([p, p, p, p, i, i, p], i),
+        "wsa_ensure_layout": ([p, p, p, p, i, i, p, ip], i),
         "wsa_plan_device_status": ([p, ip], i),
         "wsa_attention_noalloc": ([i] * 8 + [p, p, p, p, i, i, f, p], i),
+        "wsa_noalloc_device_status": ([ip], i),
         "wsa_attention_text_workspace": ([p, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)], i),
         "wsa_attention_text": ([p] + [p] * 8 + [i, i, i, i, i, f, p, ctypes.c_size_t, p], i),
         "wsa_sp_owners": ([i] * 9 + [ip, i, ip], i),
         "wsa_sp_local_rows": ([i] * 10 + [ip, i, ip], i),
-        "wsa_sp_plan_a": ([i] * 11 + [ctypes.POINTER(ctypes.c_longlong), ip, i, ip, i, ip, ip, ip], i),
+        "wsa_sp_plan_a": ([i] * 11 + [ctypes.POINTER(ctypes.c_longlong), ip, i, ip, i, ip, i, ip, ip, ip], i),
+        "wsa_sp_crossover": ([i] * 10 + [ctypes.c_double, p], i),
         "wsa_gather_rows": ([p, i, p, p, i, i, i, p], i),
         "wsa_debug_withhold_units": ([i], i),
         "wsa_rope": ([p, p, p, p, p, i, i, i, i, i, i, f, p], i),
@@ -268,6 +271,25 @@ def transition(src, dst, x, out=None, stream=None):
     return out
 
 
+def ensure_layout(current, required, x, out=None, stream=None):
+    """wsa_ensure_layout: the rows of x (packed order of plan ``current``) in
+    the packed order of plan ``required``.  Returns x itself when both plans
+    describe the same windows (nothing is launched), else ``out`` (allocated
+    if None) holding the transitioned rows."""
+    if not x.is_cuda or not x.is_contiguous() or x.dim() != 2:
+        raise WsaError(-1, "x must be a contiguous 2-D CUDA tensor")
+    if x.shape[0] != current.num_tokens:
+        raise WsaError(-1, "x row count does not match the plan")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise WsaError(-1, "out must match x")
+    moved = ctypes.c_int()
+    _check(lib.wsa_ensure_layout(current.handle, required.handle, _ptr(x), _ptr(out), x.shape[1], _dtype_code(x),
+                                 _stream(stream), ctypes.byref(moved)))
+    return out if moved.value else x
+
+
 def _rope_args(q, k, q_out, k_out):
     for t in (q, k):
         if t is not None and (not t.is_cuda or not t.is_contiguous() or t.dim() != 3):
@@ -347,8 +369,17 @@ def attention_noalloc(T, H, W, nt, nh, nw, layout, q, k, v, out, canonical=True,
     return out
 
 
+def noalloc_device_status():
+    """wsa_noalloc_device_status: synchronises; returns 0 or raises WsaError
+    with the code the last allocation-free call's kernels recorded."""
+    code = ctypes.c_int()
+    _check(lib.wsa_noalloc_device_status(ctypes.byref(code)))
+    return code.value
+
+
 __all__ = [
-    "REGULAR", "SHIFTED", "BF16", "FP32", "WsaError", "Plan", "attention", "transition",
-    "window_size", "layout_windows", "version", "lib", "attention_noalloc", "attention_text",
+    "REGULAR", "SHIFTED", "BF16", "FP32", "WsaError", "Plan", "attention", "transition", "ensure_layout",
+    "window_size", "layout_windows", "version", "lib", "attention_noalloc", "noalloc_device_status",
+    "attention_text",
     "attention_text_workspace_bytes", "gather_rows", "rope", "rope_text",
 ]

@@ -60,6 +60,7 @@ wsa_status wsa_attention(wsa_plan_t plan, const void* q, const void* k, const vo
 
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  plan->stream = s;
   if (dtype == WSA_FP32) {
     e = launch_attention_fp32(*plan, static_cast<const float*>(q), static_cast<const float*>(k),
                               static_cast<const float*>(v), static_cast<float*>(o), heads, head_dim,
@@ -123,6 +124,7 @@ wsa_status wsa_attention_text(wsa_plan_t plan, const void* q, const void* k, con
   if (e != cudaSuccess) return cuda_fail(e, "wsa_attention_text: cudaGetDevice");
   if (dev != plan->device) return fail(WSA_ERR_INVALID_ARG, "plan was created on another device");
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+  plan->stream = static_cast<cudaStream_t>(stream);
   e = launch_attention_text_bf16_tc(*plan, q, k, v, o, q_txt, k_txt, v_txt, o_txt, n_text, heads,
                                     in_order_canonical == 1, scale, workspace, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "wsa_attention_text: launch");
@@ -177,6 +179,7 @@ wsa_status wsa_rope(wsa_plan_t plan, const void* q, const void* k, void* q_out, 
   if (dev != plan->device) return fail(WSA_ERR_INVALID_ARG, "plan was created on another device");
   const void* x[2] = {q, k};
   void* y[2] = {q_out, k_out};
+  plan->stream = static_cast<cudaStream_t>(stream);
   e = launch_rope(plan, in_order_canonical == 1, x, y, k ? 2 : 1, plan->num_tokens, heads, head_dim,
                   dtype == WSA_BF16, text_len, rope_dim, theta > 0.f ? theta : 10000.0,
                   static_cast<cudaStream_t>(stream));
@@ -217,9 +220,27 @@ wsa_status wsa_transition(wsa_plan_t src, wsa_plan_t dst, const void* x_src, voi
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "wsa_transition: cudaGetDevice");
   if (dev != src->device) return fail(WSA_ERR_INVALID_ARG, "plans were created on another device");
+  src->stream = dst->stream = static_cast<cudaStream_t>(stream);
   e = launch_transition(*src, *dst, x_src, x_dst, row_bytes, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "wsa_transition: launch");
   return WSA_OK;
+}
+
+wsa_status wsa_ensure_layout(wsa_plan_t current, wsa_plan_t required, const void* x, void* x_out, int channels,
+                             wsa_dtype dtype, void* stream, int* moved) {
+  if (!current || !required || !moved) return fail(WSA_ERR_INVALID_ARG, "plans and moved must be non-null");
+  *moved = 0;
+  if (current->T != required->T || current->H != required->H || current->W != required->W)
+    return fail(WSA_ERR_MISMATCH, "plans describe different grids");
+  // The windows of a plan follow from the grid, the window size and the
+  // layout, so equal triples mean identical packed orders.
+  if (current->layout == required->layout && current->wt == required->wt && current->wh == required->wh &&
+      current->ww == required->ww)
+    return WSA_OK;
+  if (!x_out) return fail(WSA_ERR_INVALID_ARG, "the layouts differ: x_out must be given");
+  const wsa_status st = wsa_transition(current, required, x, x_out, channels, dtype, stream);
+  if (st == WSA_OK) *moved = 1;
+  return st;
 }
 
 }  // extern "C"

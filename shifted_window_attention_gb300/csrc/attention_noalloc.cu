@@ -39,14 +39,16 @@ constexpr size_t kOffDims = kOffOffsets + pad64(kNoAllocMaxWindows + 1);
 constexpr size_t kOffIds = kOffDims + pad64(6 * static_cast<size_t>(kNoAllocMaxWindows));
 constexpr size_t kOffPos = kOffIds + pad64(kNoAllocMaxTokens);
 constexpr size_t kOffItems = kOffPos + pad64(kNoAllocMaxTokens);
-constexpr size_t kScratchWords = kOffItems + pad64(2 * static_cast<size_t>(kNoAllocMaxItems));  // ~4.4 MB
+constexpr size_t kItemWords = sizeof(WorkItem) / sizeof(int);
+constexpr size_t kScratchWords = kOffItems + pad64(kItemWords * kNoAllocMaxItems);  // ~4.6 MB
 
 // Every device that loads the library holds this array until the process exits.
 static __device__ __align__(256) int g_noalloc_scratch[kScratchWords];
 
 // Device address of the scratch array on the current device.  The array's
 // name in host code is only a host-side stand-in, so the address is looked up
-// once per device with that device current and cached.
+// once per device with that device current and cached for the life of the
+// process (a device reset, which destroys the array, ends that life).
 wsa_status scratch_address(int device, int** out) {
   static std::mutex mu;
   static std::vector<int*> cache;
@@ -158,4 +160,32 @@ extern "C" wsa_status wsa_attention_noalloc(int T, int H, int W, int nt, int nh,
     e = launch_attention_bf16_tc(view, q, k, v, o, heads, in_order_canonical == 1, scale, s);
   if (e != cudaSuccess) return cuda_fail(e, "wsa_attention_noalloc: launch");
   return WSA_OK;
+}
+
+extern "C" wsa_status wsa_noalloc_device_status(int* code) {
+  if (!code) return fail(WSA_ERR_INVALID_ARG, "code is null");
+  *code = 0;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_noalloc_device_status: cudaGetDevice");
+  int* base = nullptr;
+  wsa_status st = scratch_address(dev, &base);
+  if (st != WSA_OK) return st;
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_noalloc_device_status: synchronize");
+  // WS_ERROR and WS_BOUNDS are adjacent words of the array: read and clear both.
+  static_assert(WS_BOUNDS == WS_ERROR + 1, "error words must be adjacent");
+  int words[2] = {0, 0};
+  int* err = base + kOffWork + WS_ERROR;
+  e = cudaMemcpy(words, err, sizeof(words), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_noalloc_device_status: read");
+  *code = words[0] != 0 ? words[0] : words[1];
+  if (*code == 0) return WSA_OK;
+  const int zero[2] = {0, 0};
+  e = cudaMemcpy(err, zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_noalloc_device_status: clear");
+  if (words[0] != 0)
+    return fail(WSA_ERR_DEVICE_CHECK, "a kernel recorded device error code " + std::to_string(words[0]));
+  return fail(WSA_ERR_DEVICE_CHECK, "a table held a row index out of range (device code " +
+                                        std::to_string(words[1]) + ", bounds-checked build)");
 }

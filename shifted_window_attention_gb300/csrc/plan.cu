@@ -114,31 +114,37 @@ void layout_boxes(int T, int H, int W, int wt, int wh, int ww, bool shifted,
       }
 }
 
-// Work items of `rows` query rows per item, in LPT order: heaviest first
-// (query tiles x key tiles), ties by (window, q_start) -- the ordering rule of
-// the note's "Planner" section applied to kernel work units.
+// Work items of `rows` query rows per item.  Windows are taken in LPT order
+// -- heaviest first by (query tiles x key tiles) summed over the window's
+// items, ties by window id: the ordering rule of the note's "Planner" section
+// applied to kernel work -- and each window's items follow one another in
+// query order, its last (partial) item included.  The tensor-core kernel
+// hands out every item for all heads in turn, so all query chunks of a
+// window run close together and read its keys and values while they are
+// still in L2.  (Sorting items rather than windows by cost put the windows'
+// partial chunks at the end of the list, where they re-read their windows'
+// keys and values from DRAM: 0.8 GB per 720p layer.)
 std::vector<WorkItem> make_items(const std::vector<int>& offsets, int rows, int tile) {
   struct Keyed {
     long long cost;
-    WorkItem it;
+    int window;
   };
-  std::vector<Keyed> v;
+  std::vector<Keyed> win;
   const int nwin = static_cast<int>(offsets.size()) - 1;
   for (int w = 0; w < nwin; ++w) {
     const int n = offsets[w + 1] - offsets[w];
-    const long long kv_tiles = ceil_div(n, tile);
-    for (int q0 = 0; q0 < n; q0 += rows) {
-      const long long q_tiles = ceil_div(std::min(rows, n - q0), tile);
-      v.push_back({q_tiles * kv_tiles, {w, q0}});
-    }
+    if (n <= 0) continue;
+    win.push_back({ceil_div(n, tile) * ceil_div(n, tile), w});
   }
-  std::stable_sort(v.begin(), v.end(), [](const Keyed& a, const Keyed& b) {
+  std::stable_sort(win.begin(), win.end(), [](const Keyed& a, const Keyed& b) {
     if (a.cost != b.cost) return a.cost > b.cost;
-    return std::make_pair(a.it.window, a.it.q_start) < std::make_pair(b.it.window, b.it.q_start);
+    return a.window < b.window;
   });
   std::vector<WorkItem> out;
-  out.reserve(v.size());
-  for (const auto& k : v) out.push_back(k.it);
+  for (const auto& k : win) {
+    const int n = offsets[k.window + 1] - offsets[k.window];
+    for (int q0 = 0; q0 < n; q0 += rows) out.push_back({k.window, q0});
+  }
   return out;
 }
 
@@ -288,10 +294,13 @@ wsa_status wsa_plan_create(int T, int H, int W, int nt, int nh, int nw, wsa_layo
     delete p;
     return fail(WSA_ERR_OOM, "wsa_plan_create: device allocation failed (forced by wsa_debug_fail_allocations)");
   }
-  if (e == cudaSuccess) e = cudaMalloc(&p->d_block, total);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  p->stream = s;
+  // stream-ordered: no device-wide synchronisation, ready in stream order
+  if (e == cudaSuccess) e = cudaMallocAsync(&p->d_block, total, s);
   if (e != cudaSuccess) {
     delete p;
-    return cuda_fail(e, "wsa_plan_create: cudaMalloc");
+    return cuda_fail(e, "wsa_plan_create: cudaMallocAsync");
   }
   char* base = static_cast<char*>(p->d_block);
   p->d_offsets = reinterpret_cast<int*>(base + off_offsets);
@@ -302,7 +311,6 @@ wsa_status wsa_plan_create(int T, int H, int W, int nt, int nh, int nw, wsa_layo
   p->d_simt_items = reinterpret_cast<WorkItem*>(base + off_simt);
   p->d_work = reinterpret_cast<int*>(base + off_work);
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Host sources are pageable vectors: cudaMemcpyAsync from pageable memory
   // copies out of them before returning, so they may go out of scope.
   e = cudaMemcpyAsync(p->d_offsets, p->h_offsets.data(), p->h_offsets.size() * sizeof(int),
@@ -318,7 +326,7 @@ wsa_status wsa_plan_create(int T, int H, int W, int nt, int nh, int nw, wsa_layo
   if (e == cudaSuccess) e = cudaMemsetAsync(p->d_work, 0, WS_WORDS * sizeof(int), s);
   if (e == cudaSuccess) e = launch_plan_tables(*p, s);
   if (e != cudaSuccess) {
-    cudaFree(p->d_block);
+    cudaFreeAsync(p->d_block, s);
     delete p;
     return cuda_fail(e, "wsa_plan_create: upload / plan kernel");
   }
@@ -329,9 +337,11 @@ wsa_status wsa_plan_create(int T, int H, int W, int nt, int nh, int nw, wsa_layo
 wsa_status wsa_plan_destroy(wsa_plan_t plan) {
   if (!plan) return fail(WSA_ERR_INVALID_ARG, "plan is null");
   cudaError_t e = cudaSuccess;
-  if (plan->d_block) e = cudaFree(plan->d_block);
+  // released in the order of the plan's latest call: later work on that
+  // stream may reuse the memory, earlier work has finished with it
+  if (plan->d_block) e = cudaFreeAsync(plan->d_block, plan->stream);
   delete plan;
-  if (e != cudaSuccess) return cuda_fail(e, "wsa_plan_destroy: cudaFree");
+  if (e != cudaSuccess) return cuda_fail(e, "wsa_plan_destroy: cudaFreeAsync");
   return WSA_OK;
 }
 
@@ -360,17 +370,22 @@ wsa_status wsa_plan_tables(wsa_plan_t plan, const int** offsets, const int** dim
 
 wsa_status wsa_plan_device_status(wsa_plan_t plan, int* code) {
   if (!plan || !code) return fail(WSA_ERR_INVALID_ARG, "plan or code is null");
-  cudaError_t e = cudaDeviceSynchronize();
+  // Every launch that can record an error in this plan ran on the stream of
+  // the plan's latest call or was ordered before it (one stream per plan).
+  const cudaStream_t s = plan->stream;
+  cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "wsa_plan_device_status: synchronize");
   // WS_ERROR and WS_BOUNDS are adjacent words: read and clear both.
   static_assert(WS_BOUNDS == WS_ERROR + 1, "error words must be adjacent");
   int words[2] = {0, 0};
-  e = cudaMemcpy(words, plan->d_work + WS_ERROR, sizeof(words), cudaMemcpyDeviceToHost);
+  e = cudaMemcpyAsync(words, plan->d_work + WS_ERROR, sizeof(words), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "wsa_plan_device_status: read");
   *code = words[0] != 0 ? words[0] : words[1];
   if (*code != 0) {
     const int zero[2] = {0, 0};
-    e = cudaMemcpy(plan->d_work + WS_ERROR, zero, sizeof(zero), cudaMemcpyHostToDevice);
+    e = cudaMemcpyAsync(plan->d_work + WS_ERROR, zero, sizeof(zero), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "wsa_plan_device_status: clear");
     if (words[0] != 0)
       return fail(WSA_ERR_DEVICE_CHECK, "a kernel recorded device error code " + std::to_string(words[0]));

@@ -116,6 +116,60 @@ void assign_rows(const Layout& L, const std::vector<int>& owner, int ranks, std:
   }
 }
 
+// C[s * ranks + d] = rows that rank d holds in the destination layout and
+// rank s holds in the source layout.
+std::vector<long long> count_matrix(const std::vector<int>& src_rank, const std::vector<int>& dst_rank, int ranks) {
+  std::vector<long long> C(static_cast<size_t>(ranks) * ranks, 0);
+  for (size_t id = 0; id < src_rank.size(); ++id) ++C[static_cast<size_t>(src_rank[id]) * ranks + dst_rank[id]];
+  return C;
+}
+
+bool crosses(const std::vector<long long>& C, int ranks) {
+  for (int s = 0; s < ranks; ++s)
+    for (int d = 0; d < ranks; ++d)
+      if (s != d && C[static_cast<size_t>(s) * ranks + d] != 0) return true;
+  return false;
+}
+
+// Plan B under this library's reading: hidden rows stay with the regular
+// layout's owners; shifted window w runs on the rank holding most of its
+// rows (lowest id on ties), which receives the others (halo) and sends
+// their outputs back.
+struct PlanBCounts {
+  std::vector<int> window_rank;
+  std::vector<long long> halo_in, halo_out, tokens;
+  std::vector<double> work;  // sum of n_w^2 of the windows a rank computes
+};
+
+PlanBCounts plan_b_counts(const Layout& R, const Layout& S, int ranks) {
+  const std::vector<int> own = lpt_owner(R, ranks);
+  std::vector<int> holder, unused;
+  std::vector<long long> held;
+  assign_rows(R, own, ranks, &holder, &unused, &held);
+  PlanBCounts b;
+  b.window_rank.assign(S.num_windows(), 0);
+  b.halo_in.assign(ranks, 0);
+  b.halo_out.assign(ranks, 0);
+  b.tokens.assign(ranks, 0);
+  b.work.assign(ranks, 0.0);
+  std::vector<long long> share(ranks, 0);
+  for (int w = 0; w < S.num_windows(); ++w) {
+    std::fill(share.begin(), share.end(), 0);
+    S.for_each_id(w, [&](int id) { ++share[holder[id]]; });
+    int best = 0;  // the rank holding most rows; the lowest id on ties
+    for (int r = 1; r < ranks; ++r)
+      if (share[r] > share[best]) best = r;
+    const long long n = S.window_tokens(w);
+    b.halo_in[best] += n - share[best];
+    for (int r = 0; r < ranks; ++r)
+      if (r != best) b.halo_out[r] += share[r];
+    b.tokens[best] += n;
+    b.work[best] += static_cast<double>(n) * static_cast<double>(n);
+    b.window_rank[w] = best;
+  }
+  return b;
+}
+
 wsa_status check_ranks(int ranks, int rank) {
   if (ranks <= 0) return fail(WSA_ERR_INVALID_ARG, "ranks must be > 0");
   if (rank < 0 || rank >= ranks) return fail(WSA_ERR_INVALID_ARG, "rank must be in [0, ranks)");
@@ -169,8 +223,8 @@ wsa_status wsa_sp_local_rows(int T, int H, int W, int nt, int nh, int nw, wsa_la
 
 wsa_status wsa_sp_plan_a(int T, int H, int W, int nt, int nh, int nw, wsa_layout src_layout,
                          wsa_layout dst_layout, int max_temporal, int ranks, int rank, long long* counts,
-                         int* send_index, int send_capacity, int* recv_index, int recv_capacity, int* n_send,
-                         int* n_recv, int* network_exchange_required) {
+                         int* send_index, int send_capacity, int* recv_index, int recv_capacity, int* local_index,
+                         int local_capacity, int* n_send, int* n_recv, int* network_exchange_required) {
   if (!n_send || !n_recv || !network_exchange_required)
     return fail(WSA_ERR_INVALID_ARG, "n_send, n_recv and network_exchange_required must be non-null");
   wsa_status st = check_ranks(ranks, rank);
@@ -186,16 +240,8 @@ wsa_status wsa_sp_plan_a(int T, int H, int W, int nt, int nh, int nw, wsa_layout
   assign_rows(S, own_s, ranks, &src_rank, &src_local, &src_held);
   assign_rows(D, own_d, ranks, &dst_rank, &dst_local, &dst_held);
 
-  // the global count matrix, C[s][d] = rows rank d needs from rank s
-  std::vector<long long> C(static_cast<size_t>(ranks) * ranks, 0);
-  for (long long id = 0; id < S.N; ++id) ++C[static_cast<size_t>(src_rank[id]) * ranks + dst_rank[id]];
-  bool cross = false;
-  for (int s = 0; s < ranks && !cross; ++s)
-    for (int d = 0; d < ranks; ++d)
-      if (s != d && C[static_cast<size_t>(s) * ranks + d] != 0) {
-        cross = true;
-        break;
-      }
+  const std::vector<long long> C = count_matrix(src_rank, dst_rank, ranks);
+  const bool cross = crosses(C, ranks);
   *network_exchange_required = cross ? 1 : 0;
   *n_send = static_cast<int>(src_held[rank]);
   *n_recv = static_cast<int>(dst_held[rank]);
@@ -204,26 +250,36 @@ wsa_status wsa_sp_plan_a(int T, int H, int W, int nt, int nh, int nw, wsa_layout
     return fail(WSA_ERR_INVALID_ARG, "send_index capacity is smaller than the rank's source row count");
   if (recv_index && recv_capacity < *n_recv)
     return fail(WSA_ERR_INVALID_ARG, "recv_index capacity is smaller than the rank's destination row count");
+  if (local_index && !cross && local_capacity < *n_recv)
+    return fail(WSA_ERR_INVALID_ARG, "local_index capacity is smaller than the rank's destination row count");
+  if (!send_index && !recv_index && !local_index) return WSA_OK;
 
-  if (send_index) {
-    // segments by destination rank; inside one, destination-local order:
-    // walk each destination rank's rows in its order, keep those held here
+  // segments by destination rank; inside one, destination-local order:
+  // walk each destination rank's rows in its order, keep those held here
+  std::vector<int> send(static_cast<size_t>(*n_send));
+  {
     long long k = 0;
     for (int d = 0; d < ranks; ++d)
       for (int w = 0; w < D.num_windows(); ++w)
         if (own_d[w] == d)
           D.for_each_id(w, [&](int id) {
-            if (src_rank[id] == rank) send_index[k++] = src_local[id];
+            if (src_rank[id] == rank) send[k++] = src_local[id];
           });
   }
-  if (recv_index) {
+  std::vector<int> recv(static_cast<size_t>(*n_recv));
+  {
     std::vector<long long> next(ranks, 0);  // next receive row of each source segment
     for (int s = 1; s < ranks; ++s) next[s] = next[s - 1] + C[static_cast<size_t>(s - 1) * ranks + rank];
     long long p = 0;
     for (int w = 0; w < D.num_windows(); ++w)
-      if (own_d[w] == rank)
-        D.for_each_id(w, [&](int id) { recv_index[p++] = static_cast<int>(next[src_rank[id]]++); });
+      if (own_d[w] == rank) D.for_each_id(w, [&](int id) { recv[p++] = static_cast<int>(next[src_rank[id]]++); });
   }
+  if (send_index) std::copy(send.begin(), send.end(), send_index);
+  if (recv_index) std::copy(recv.begin(), recv.end(), recv_index);
+  // No row changes rank: every receive row comes from this rank's own send
+  // buffer, so the two gathers compose into one through send[recv[p]].
+  if (local_index && !cross)
+    for (size_t p = 0; p < recv.size(); ++p) local_index[p] = send[static_cast<size_t>(recv[p])];
   return WSA_OK;
 }
 
@@ -240,31 +296,87 @@ wsa_status wsa_sp_plan_b(int T, int H, int W, int nt, int nh, int nw, int max_te
   *num_windows = S.num_windows();
   if (window_rank && capacity < S.num_windows())
     return fail(WSA_ERR_INVALID_ARG, "window_rank capacity is smaller than the shifted window count");
-  const std::vector<int> own = lpt_owner(R, ranks);
-  std::vector<int> holder, unused;
-  std::vector<long long> held;
-  assign_rows(R, own, ranks, &holder, &unused, &held);
-  std::vector<long long> in(ranks, 0), out(ranks, 0), tok(ranks, 0), share(ranks, 0);
-  std::vector<double> wk(ranks, 0.0);
-  for (int w = 0; w < S.num_windows(); ++w) {
-    std::fill(share.begin(), share.end(), 0);
-    S.for_each_id(w, [&](int id) { ++share[holder[id]]; });
-    int best = 0;  // the rank holding most rows; the lowest id on ties
-    for (int r = 1; r < ranks; ++r)
-      if (share[r] > share[best]) best = r;
-    const long long n = S.window_tokens(w);
-    in[best] += n - share[best];
-    for (int r = 0; r < ranks; ++r)
-      if (r != best) out[r] += share[r];
-    tok[best] += n;
-    wk[best] += static_cast<double>(n) * static_cast<double>(n);
-    if (window_rank) window_rank[w] = best;
-  }
+  const PlanBCounts b = plan_b_counts(R, S, ranks);
+  if (window_rank) std::copy(b.window_rank.begin(), b.window_rank.end(), window_rank);
   for (int r = 0; r < ranks; ++r) {
-    if (halo_in) halo_in[r] = in[r];
-    if (halo_out) halo_out[r] = out[r];
-    if (tokens) tokens[r] = tok[r];
-    if (work) work[r] = wk[r];
+    if (halo_in) halo_in[r] = b.halo_in[r];
+    if (halo_out) halo_out[r] = b.halo_out[r];
+    if (tokens) tokens[r] = b.tokens[r];
+    if (work) work[r] = b.work[r];
+  }
+  return WSA_OK;
+}
+
+wsa_status wsa_sp_crossover(int T, int H, int W, int nt, int nh, int nw, int max_temporal, int ranks, int channels,
+                            int bytes_per_elem, double shifted_ms, wsa_sp_crossover_t* out) {
+  if (!out) return fail(WSA_ERR_INVALID_ARG, "out is null");
+  if (ranks <= 0) return fail(WSA_ERR_INVALID_ARG, "ranks must be > 0");
+  if (channels <= 0 || bytes_per_elem <= 0) return fail(WSA_ERR_INVALID_ARG, "channels and bytes_per_elem must be > 0");
+  if (!(shifted_ms == shifted_ms)) return fail(WSA_ERR_INVALID_ARG, "shifted_ms is NaN");
+  Layout R, S;
+  wsa_status st = make_layout(T, H, W, nt, nh, nw, WSA_REGULAR, max_temporal, &R);
+  if (st != WSA_OK) return st;
+  st = make_layout(T, H, W, nt, nh, nw, WSA_SHIFTED, max_temporal, &S);
+  if (st != WSA_OK) return st;
+  const long long row = static_cast<long long>(channels) * bytes_per_elem;
+  const std::vector<int> own_r = lpt_owner(R, ranks), own_s = lpt_owner(S, ranks);
+  std::vector<int> rank_r, rank_s, local_unused;
+  std::vector<long long> held_unused;
+  assign_rows(R, own_r, ranks, &rank_r, &local_unused, &held_unused);
+  assign_rows(S, own_s, ranks, &rank_s, &local_unused, &held_unused);
+  // Plan A: the rows that change rank at the regular -> shifted and the
+  // shifted -> regular boundary (off-diagonal counts); the busiest rank is
+  // the larger of its rows sent and its rows received.
+  long long a_rows = 0, a_max = 0;
+  for (int dir = 0; dir < 2; ++dir) {
+    const std::vector<long long> C = dir == 0 ? count_matrix(rank_r, rank_s, ranks) : count_matrix(rank_s, rank_r, ranks);
+    long long busiest = 0;
+    for (int r = 0; r < ranks; ++r) {
+      long long sent = 0, recv = 0;
+      for (int q = 0; q < ranks; ++q)
+        if (q != r) {
+          sent += C[static_cast<size_t>(r) * ranks + q];
+          recv += C[static_cast<size_t>(q) * ranks + r];
+        }
+      a_rows += sent;
+      busiest = std::max(busiest, std::max(sent, recv));
+    }
+    a_max += busiest;
+  }
+  // Plan B: halo rows in before the shifted layer and their outputs back after it.
+  const PlanBCounts b = plan_b_counts(R, S, ranks);
+  long long b_in = 0, b_busiest = 0;
+  for (int r = 0; r < ranks; ++r) {
+    b_in += b.halo_in[r];
+    b_busiest = std::max(b_busiest, std::max(b.halo_in[r], b.halo_out[r]));
+  }
+  // shifted-layer attention work per rank: Plan A's LPT owners against Plan B's computing ranks
+  std::vector<double> a_work(ranks, 0.0);
+  double total = 0.0;
+  for (int w = 0; w < S.num_windows(); ++w) {
+    const double n = static_cast<double>(S.window_tokens(w));
+    a_work[own_s[w]] += n * n;
+    total += n * n;
+  }
+  const double a_peak = *std::max_element(a_work.begin(), a_work.end());
+  const double b_peak = *std::max_element(b.work.begin(), b.work.end());
+  const double mean = total / ranks;
+  out->plan_a_bytes = a_rows * row;
+  out->plan_a_max_rank_bytes = a_max * row;
+  out->plan_b_bytes = 2 * b_in * row;
+  out->plan_b_max_rank_bytes = 2 * b_busiest * row;
+  out->plan_a_shifted_imbalance = mean > 0 ? a_peak / mean : 1.0;
+  out->plan_b_shifted_imbalance = mean > 0 ? b_peak / mean : 1.0;
+  out->plan_a_shifted_ms_max_rank = -1.0;
+  out->plan_b_shifted_ms_max_rank = -1.0;
+  out->crossover_link_gbs = -1.0;
+  if (shifted_ms > 0 && total > 0) {
+    // each plan's busiest-rank attention time as its share of the one-GPU time
+    const double ta = shifted_ms * a_peak / total, tb = shifted_ms * b_peak / total;
+    out->plan_a_shifted_ms_max_rank = ta;
+    out->plan_b_shifted_ms_max_rank = tb;
+    const double dbytes = static_cast<double>(out->plan_a_max_rank_bytes - out->plan_b_max_rank_bytes);
+    if (tb > ta && dbytes > 0) out->crossover_link_gbs = dbytes / ((tb - ta) * 1e-3) / 1e9;
   }
   return WSA_OK;
 }

@@ -28,7 +28,8 @@ struct WorkItem {
 
 // Host geometry of a layout (plan.cu): window size, window boxes
 // (t0,t1,h0,h1,w0,w1 per window, enumeration order) and the attention work
-// items of `rows` query rows in heaviest-first order.
+// items of `rows` query rows: windows heaviest first, each window's items
+// together.
 wsa_status window_size(int T, int H, int W, int nt, int nh, int nw, int max_temporal, int* wt, int* wh,
                        int* ww);
 void layout_boxes(int T, int H, int W, int wt, int wh, int ww, bool shifted, std::vector<int>* dims);
@@ -74,6 +75,9 @@ struct wsa_plan_s {
   std::vector<int> h_dims;     // [num_windows * 6]
   int num_tc_items = 0;
   int num_simt_items = 0;
+  // Stream of the plan's latest call (creation, then every launch that uses
+  // the plan): its status read and its release are ordered on it.
+  cudaStream_t stream = nullptr;
   // device memory: one allocation carved into the tables below
   void* d_block = nullptr;
   int* d_offsets = nullptr;

@@ -61,14 +61,18 @@ class PlanA:
         n_send, n_recv, cross = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
         args = (T, H, W, nt, nh, nw, src_layout, dst_layout, max_temporal, ranks, rank)
         cp = counts.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong))
-        _check(lib.wsa_sp_plan_a(*args, cp, None, 0, None, 0, ctypes.byref(n_send), ctypes.byref(n_recv),
+        _check(lib.wsa_sp_plan_a(*args, cp, None, 0, None, 0, None, 0, ctypes.byref(n_send), ctypes.byref(n_recv),
                                  ctypes.byref(cross)))
         self.send_index = np.zeros(n_send.value, dtype=np.int32)
         self.recv_index = np.zeros(n_recv.value, dtype=np.int32)
+        # the fast path's composed index (filled by the planner when no row changes rank)
+        self.local_index = np.zeros(0 if cross.value else n_recv.value, dtype=np.int32)
         ip = ctypes.POINTER(ctypes.c_int)
         _check(lib.wsa_sp_plan_a(*args, cp, self.send_index.ctypes.data_as(ip), n_send.value,
-                                 self.recv_index.ctypes.data_as(ip), n_recv.value, ctypes.byref(n_send),
-                                 ctypes.byref(n_recv), ctypes.byref(cross)))
+                                 self.recv_index.ctypes.data_as(ip), n_recv.value,
+                                 self.local_index.ctypes.data_as(ip) if not cross.value else None,
+                                 self.local_index.size, ctypes.byref(n_send), ctypes.byref(n_recv),
+                                 ctypes.byref(cross)))
         self.counts = counts
         self.network_exchange_required = bool(cross.value)
         self.input_split_sizes = [int(c) for c in counts[rank]]
@@ -78,12 +82,12 @@ class PlanA:
 
     def device_tables(self, device):
         """(send_index, recv_index, local_index) as int32 tensors on ``device``;
-        local_index = send_index[recv_index], the fast path's single gather."""
+        local_index is the planner's composed index of the fast path (empty
+        when rows change rank)."""
         key = torch.device(device)
         if key not in self._dev:
-            local = self.send_index[self.recv_index] if not self.network_exchange_required else np.zeros(0, np.int32)
-            self._dev[key] = tuple(torch.from_numpy(np.ascontiguousarray(a)).to(key)
-                                   for a in (self.send_index, self.recv_index, local))
+            self._dev[key] = tuple(torch.from_numpy(a).to(key)
+                                   for a in (self.send_index, self.recv_index, self.local_index))
         return self._dev[key]
 
     def pack(self, x_local, out=None, stream=None):
@@ -138,59 +142,30 @@ def plan_b(T, H, W, nt, nh, nw, ranks, max_temporal=30):
     return {"window_rank": wr, "work": work, **arrs}
 
 
+class _Crossover(ctypes.Structure):
+    _fields_ = [("plan_a_bytes", ctypes.c_longlong), ("plan_a_max_rank_bytes", ctypes.c_longlong),
+                ("plan_b_bytes", ctypes.c_longlong), ("plan_b_max_rank_bytes", ctypes.c_longlong),
+                ("plan_a_shifted_imbalance", ctypes.c_double), ("plan_b_shifted_imbalance", ctypes.c_double),
+                ("plan_a_shifted_ms_max_rank", ctypes.c_double), ("plan_b_shifted_ms_max_rank", ctypes.c_double),
+                ("crossover_link_gbs", ctypes.c_double)]
+
+
 def crossover(T, H, W, nt, nh, nw, ranks, channels, bytes_per_elem=2, max_temporal=30, shifted_ms=None):
-    """The Plan A / Plan B comparison for one regular + shifted layer pair.
-
-    Plan A moves the rows that change rank at both boundaries (off-diagonal
-    counts of each wsa_sp_plan_a matrix).  Plan B moves the halo rows in and
-    their outputs back around the shifted layer.  Rows count as hidden-state
-    rows of ``channels`` elements.  Also reported: the busiest rank's traffic
-    (it bounds the all-to-all time) and the attention work imbalance of the
-    shifted layer (max over mean of sum n_w^2; Plan A balances it by LPT on
-    tokens).
-
-    With ``shifted_ms``, the measured one-GPU time of the shifted attention
-    layer, the busiest rank's attention time is estimated under each plan as
-    shifted_ms times its share of the total sum of n_w^2.  The result then
-    includes the link bandwidth below which Plan B's smaller exchange
-    outweighs its imbalance: the difference in the busiest rank's bytes
-    divided by the difference in the busiest rank's attention time."""
-    row = channels * bytes_per_elem
-    a_rows, a_max = 0, 0
-    for src, dst in ((0, 1), (1, 0)):
-        c = PlanA(T, H, W, nt, nh, nw, src, dst, ranks, 0, max_temporal).counts
-        off = c - np.diag(np.diag(c))
-        a_rows += int(off.sum())
-        a_max += int(max(off.sum(axis=1).max(), off.sum(axis=0).max()))
-    b = plan_b(T, H, W, nt, nh, nw, ranks, max_temporal)
-    b_rows = 2 * int(b["halo_in"].sum())
-    b_max = 2 * int(max(b["halo_in"].max(), b["halo_out"].max()))
-    # Plan A's shifted-layer work per rank under its own LPT assignment
-    own = owners(T, H, W, nt, nh, nw, 1, ranks, max_temporal)
-    n = np.array([(b1 - b0) * (h1 - h0) * (w1 - w0) for (b0, b1, h0, h1, w0, w1) in
-                  _boxes(T, H, W, nt, nh, nw, 1, max_temporal)], dtype=np.float64)
-    a_work = np.bincount(own, weights=n * n, minlength=ranks)
-    extra = {}
+    """wsa_sp_crossover: Plan A against Plan B for one regular + shifted
+    layer pair (host only), as a dict of the library's figures.  With
+    ``shifted_ms`` (the measured one-GPU shifted-layer time) it also holds
+    each plan's busiest-rank attention time and ``crossover_link_gbs`` (None
+    when Plan B never wins)."""
+    c = _Crossover()
+    _check(lib.wsa_sp_crossover(T, H, W, nt, nh, nw, max_temporal, ranks, channels, bytes_per_elem,
+                                float(shifted_ms) if shifted_ms is not None else 0.0, ctypes.byref(c)))
+    out = {"ranks": ranks}
+    out.update({name: getattr(c, name) for name, _ in _Crossover._fields_[:6]})
     if shifted_ms is not None:
-        total = float(a_work.sum())
-        ta = shifted_ms * float(a_work.max()) / total
-        tb = shifted_ms * float(b["work"].max()) / total
-        dbytes = (a_max - b_max) * row
-        extra = {"plan_a_shifted_ms_max_rank": ta, "plan_b_shifted_ms_max_rank": tb,
-                 "crossover_link_gbs": dbytes / ((tb - ta) * 1e-3) / 1e9 if tb > ta and dbytes > 0 else None}
-    return {
-        **extra,
-        "ranks": ranks,
-        "plan_a_bytes": a_rows * row, "plan_a_max_rank_bytes": a_max * row,
-        "plan_b_bytes": b_rows * row, "plan_b_max_rank_bytes": b_max * row,
-        "plan_a_shifted_imbalance": float(a_work.max() / a_work.mean()),
-        "plan_b_shifted_imbalance": float(b["work"].max() / b["work"].mean()),
-    }
-
-
-def _boxes(T, H, W, nt, nh, nw, layout, max_temporal):
-    from . import layout_windows
-    return layout_windows(T, H, W, nt, nh, nw, layout, max_temporal)
+        out["plan_a_shifted_ms_max_rank"] = c.plan_a_shifted_ms_max_rank
+        out["plan_b_shifted_ms_max_rank"] = c.plan_b_shifted_ms_max_rank
+        out["crossover_link_gbs"] = c.crossover_link_gbs if c.crossover_link_gbs >= 0 else None
+    return out
 
 
 def _main():

@@ -27,3 +27,10 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    # stop the oracle worker pool of the full-size parity tests, if one was started
+    pool = sys.modules.get("tests.oracle_pool")
+    if pool is not None:
+        pool.close()

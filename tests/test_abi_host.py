@@ -113,3 +113,11 @@ def test_layout_capacity_and_null_checks(wsa):
     assert lib.wsa_plan_info(None, *([None] * 7)) == -1
     assert lib.wsa_attention(None, None, None, None, None, 1, 128, 0, 1, 0.0, None) == -1
     assert lib.wsa_transition(None, None, None, None, 8, 0, None) == -1
+
+
+def test_ensure_layout_and_noalloc_status_null_checks(wsa):
+    lib = wsa.lib
+    moved = ctypes.c_int(7)
+    assert lib.wsa_ensure_layout(None, None, None, None, 8, 0, None, ctypes.byref(moved)) == -1
+    assert lib.wsa_ensure_layout(None, None, None, None, 8, 0, None, None) == -1
+    assert lib.wsa_noalloc_device_status(None) == -1

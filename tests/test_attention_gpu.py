@@ -11,7 +11,8 @@ import torch
 
 import oracle
 import wsa_inputs
-from tests.helpers import assert_bf16_close, assert_fp32_close, to64
+from tests import oracle_pool
+from tests.helpers import BF16_MAX_ABS, BF16_REL_RMS, assert_bf16_close, assert_fp32_close, to64
 from wsa_inputs import WORKLOADS
 
 pytestmark = pytest.mark.gpu
@@ -145,54 +146,51 @@ def _sample_windows(op, count, seed):
     return sorted(picks)
 
 
-def _check_sampled(wsa, w, layout, layer=0, windows=6, heads_per_window=3, seed=0):
+def _full_layer(wsa, w, layout, layer=0, windows=None, heads=None):
+    """One layer on the GPU (canonical rows), compared with the fp64 oracle on
+    every element of the given windows and heads (all by default).  Prints
+    and returns (max_abs, rel_rms)."""
     g = _grid(w)
     p = wsa.Plan(*g, layout)
-    op = oracle.make_plan(*g, layout)
     q, k, v = wsa_inputs.qkv(w, layer=layer, device="cuda")
     o = torch.full_like(q, float("nan"))
     wsa.attention(p, q, k, v, out=o)
     assert p.device_status() == 0
     # every output row of every head was written and is finite
     assert bool(torch.isfinite(o).all())
-    qn, kn, vn, on = (t.float().cpu().numpy() for t in (q, k, v, o))
-    rng = np.random.default_rng(seed + layer)
-    worst = (0.0, 0.0)
-    for win in _sample_windows(op, windows, seed + layer):
-        n = int(op.offsets[win + 1] - op.offsets[win])
-        rows = op.ids[op.offsets[win]:op.offsets[win + 1]].astype(np.int64)
-        for h in rng.choice(w.heads, size=heads_per_window, replace=False):
-            ref = oracle.window_attention_rows(qn, kn, vn, op, win, int(h), np.arange(n))
-            e = assert_bf16_close(on[rows, int(h), :], ref, f"{w.name} L{layout} win {win} head {h}")
-            worst = (max(worst[0], e[0]), max(worst[1], e[1]))
-    return worst
+    q, k, v, o = (t.cpu() for t in (q, k, v, o))
+    op = oracle.make_plan(*g, layout)
+    max_abs, rel_rms, where, count = oracle_pool.compare_layer(q, k, v, o, op, windows=windows, heads=heads)
+    what = (f"{w.name} layer {layer} ({'shifted' if layout else 'regular'}), "
+            f"{'all' if windows is None else len(windows)} windows x {'all' if heads is None else len(heads)} heads")
+    print(f"{what}: {count} elements, max-abs {max_abs:.3e} (worst window, head {where}), rel-RMS {rel_rms:.3e}")
+    assert max_abs <= BF16_MAX_ABS and rel_rms <= BF16_REL_RMS, (
+        f"{what}: max_abs={max_abs:.3e} (<= {BF16_MAX_ABS}) at {where}, rel_rms={rel_rms:.3e} (<= {BF16_REL_RMS})")
+    return max_abs, rel_rms
 
 
 @pytest.mark.parametrize("name", ["720p", "1080p", "long"])
 @pytest.mark.parametrize("layout", [0, 1])
-def test_full_size_sampled(wsa, name, layout):
-    _check_sampled(wsa, WORKLOADS[name], layout)
+def test_every_window_and_head(wsa, name, layout):
+    # the two-layer workloads compared in full: every output element of both
+    # layouts (every window, all 24 heads) against the fp64 oracle
+    _full_layer(wsa, WORKLOADS[name], layout)
 
 
-@pytest.mark.parametrize("layout", [0, 1])
-def test_720p_every_window_and_head(wsa, layout):
-    # the headline workload compared in full: every output element of both
-    # layouts (36 / 64 windows x 24 heads) against the fp64 oracle
-    w = WORKLOADS["720p"]
-    p = wsa.Plan(*_grid(w), layout)
-    q, k, v = wsa_inputs.qkv(w, layer=0)
-    o = wsa.attention(p, q.cuda(), k.cuda(), v.cuda())
-    assert p.device_status() == 0
-    ref = oracle.window_attention(to64(q), to64(k), to64(v), oracle.make_plan(*_grid(w), layout))
-    assert_bf16_close(to64(o), ref, f"720p layout {layout}, all windows and heads")
-
-
-def test_32layer_schedule_sampled(wsa):
-    # alternating layouts, fresh Q/K/V per layer; layers 0 and 1 plus a seeded
-    # sample of later layers
+@pytest.mark.parametrize("layer", [0, 1])
+def test_32layer_first_layers_every_window_and_head(wsa, layer):
+    # the 302,400-token grid: layers 0 (regular) and 1 (shifted) in full
     w = WORKLOADS["32layer"]
-    for layer in (0, 1, 2, 13, 30, 31):
-        _check_sampled(wsa, w, layer % 2, layer=layer, windows=3, heads_per_window=2)
+    _full_layer(wsa, w, layer % 2, layer=layer)
+
+
+@pytest.mark.parametrize("layer", [2, 13, 30, 31])
+def test_32layer_later_layers_sampled(wsa, layer):
+    # later layers of the alternating schedule (fresh Q/K/V per layer): a
+    # seeded sample of 8 windows plus the smallest and largest, all heads
+    w = WORKLOADS["32layer"]
+    op = oracle.make_plan(*_grid(w), layer % 2)
+    _full_layer(wsa, w, layer % 2, layer=layer, windows=_sample_windows(op, 8, 100 + layer))
 
 
 def test_argument_errors(wsa):

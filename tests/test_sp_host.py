@@ -90,7 +90,7 @@ def test_errors(sp):
     lib = sp.lib
     n_send, n_recv, cross = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     small = (ctypes.c_int * 3)()
-    st = lib.wsa_sp_plan_a(*GRIDS["tiny"], 0, 1, 30, 2, 0, None, small, 3, None, 0, ctypes.byref(n_send),
+    st = lib.wsa_sp_plan_a(*GRIDS["tiny"], 0, 1, 30, 2, 0, None, small, 3, None, 0, None, 0, ctypes.byref(n_send),
                            ctypes.byref(n_recv), ctypes.byref(cross))
     assert st == -1 and n_send.value > 3
     n = ctypes.c_int()
@@ -132,3 +132,50 @@ def test_plan_b_errors(sp):
     small = (ctypes.c_int * 2)()
     assert sp.lib.wsa_sp_plan_b(*GRIDS["tiny"], 30, 2, small, 2, ctypes.byref(n), None, None, None, None) == -1
     assert n.value == 36
+
+
+@pytest.mark.parametrize("name", list(GRIDS))
+@pytest.mark.parametrize("layouts", [(0, 1), (1, 1)])
+def test_local_index_is_the_composed_fast_path(sp, name, layouts):
+    # one rank (and any boundary where no row changes rank): the planner's
+    # local_index equals send_index[recv_index] of the oracle's schedule
+    grid = GRIDS[name]
+    src, dst = oracle.make_plan(*grid, layouts[0]), oracle.make_plan(*grid, layouts[1])
+    ref = osp.plan_a(src, dst, 1)
+    pa = sp.PlanA(*grid, *layouts, 1, 0)
+    assert not pa.network_exchange_required
+    assert np.array_equal(pa.local_index, ref["send_index"][0][ref["recv_index"][0]])
+    # with ranks that exchange rows there is no fast-path table
+    assert sp.PlanA(*grid, 0, 1, 3, 1).local_index.size == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "odd", "720p"])
+@pytest.mark.parametrize("ranks", [1, 2, 4, 8])
+def test_crossover_figures_from_the_oracle(sp, name, ranks):
+    # every byte and imbalance figure recomputed from the oracle's Plan A
+    # matrices, LPT owners and Plan B counts
+    grid = GRIDS[name]
+    reg, sft = oracle.make_plan(*grid, 0), oracle.make_plan(*grid, 1)
+    row = 3072 * 2
+    a_rows = a_max = 0
+    for s, d in ((reg, sft), (sft, reg)):
+        c = osp.plan_a(s, d, ranks)["counts"]
+        off = c - np.diag(np.diag(c))
+        a_rows += int(off.sum())
+        a_max += int(max(off.sum(axis=1).max(), off.sum(axis=0).max()))
+    b = osp.plan_b(reg, sft, ranks)
+    n = np.diff(sft.offsets).astype(np.float64)
+    a_work = np.bincount(osp.owners(sft, ranks), weights=n * n, minlength=ranks)
+    got = sp.crossover(*grid, ranks, channels=3072, shifted_ms=2.0)
+    assert got["plan_a_bytes"] == a_rows * row and got["plan_a_max_rank_bytes"] == a_max * row
+    assert got["plan_b_bytes"] == 2 * int(b["halo_in"].sum()) * row
+    assert got["plan_b_max_rank_bytes"] == 2 * int(max(b["halo_in"].max(), b["halo_out"].max())) * row
+    assert np.isclose(got["plan_a_shifted_imbalance"], a_work.max() / a_work.mean())
+    assert np.isclose(got["plan_b_shifted_imbalance"], b["work"].max() / np.mean(b["work"]))
+    ta, tb = 2.0 * a_work.max() / a_work.sum(), 2.0 * b["work"].max() / a_work.sum()
+    assert np.isclose(got["plan_a_shifted_ms_max_rank"], ta) and np.isclose(got["plan_b_shifted_ms_max_rank"], tb)
+    dbytes = (a_max - 2 * int(max(b["halo_in"].max(), b["halo_out"].max()))) * row
+    if tb > ta and dbytes > 0:
+        assert np.isclose(got["crossover_link_gbs"], dbytes / ((tb - ta) * 1e-3) / 1e9)
+    else:
+        assert got["crossover_link_gbs"] is None
