@@ -38,17 +38,23 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) of one regular-layout attention launch of the
 # 24-head 720p workload with canonical rows: an ncu capture of the same grid
-# with 8 heads measured 885.3 MB, scaled x3 (each head's rows are disjoint, so
-# traffic grows with the head count).  Valid only for the kernel source it was
+# with 8 heads measured 601.0 MB (465.6 MB read, 135.4 MB written), scaled x3
+# (each head's rows are disjoint, so traffic grows with the head count).
+# Valid only for the kernel source and the work-list order (plan.cu) it was
 # measured on.
-MEASURED_TRAFFIC = {"kernel_sha1": "66187d7c5da48c79", "workload": "720p", "heads": 24, "bytes": 2.656e9}
+MEASURED_TRAFFIC = {"kernel_sha1": "66187d7c5da48c79", "plan_sha1": "07a46346b403002a", "workload": "720p",
+                    "heads": 24, "bytes": 1.803e9}
+
+
+def source_sha1(name):
+    import hashlib
+    path = os.path.join(ROOT, "shifted_window_attention_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:16]
 
 
 def kernel_sha1():
-    import hashlib
-    path = os.path.join(ROOT, "shifted_window_attention_gb300", "csrc", "attention_tc.cu")
-    with open(path, "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()[:16]
+    return source_sha1("attention_tc.cu")
 
 
 def attn_flops(offsets, heads, d, n_text=0):
@@ -350,29 +356,40 @@ def run_ours(args):
         comp_done = [torch.cuda.Event() for _ in range(2)]
         out_done = [torch.cuda.Event() for _ in range(2)]
         e2e_steps = max(2, args.steps)
+        # per-step timeline of the timed run: [upload start, upload end,
+        # compute start, compute end, download start, download end], each
+        # recorded on the stream that does the work
+        tl = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(e2e_steps)]
 
-        def e2e_run(n):
+        def e2e_run(n, timeline=None):
             for i in range(n):
                 b = i % 2
+                t = timeline[i] if timeline else None
                 din, dout = dev_sets[b], out_sets[b]
                 with torch.cuda.stream(s_in):
                     if i >= 2:
                         s_in.wait_event(comp_done[b])  # buffer set b no longer read by step i-2
+                    if t: t[0].record(s_in)
                     for d_, h_ in zip(din, host_in):
                         d_.copy_(h_, non_blocking=True)
+                    if t: t[1].record(s_in)
                     in_ready[b].record(s_in)
                 stream.wait_event(in_ready[b])
                 if i >= 2:
                     stream.wait_event(out_done[b])  # step i-2's outputs have left set b
                 q0, k0, v0, q1, k1, v1, x = din
+                if t: t[2].record(stream)
                 wsa.attention(plans[0], q0, k0, v0, out=dout[0], canonical=canonical)
                 wsa.transition(plans[0], plans[1], x, out=dout[2])
                 wsa.attention(plans[1], q1, k1, v1, out=dout[1], canonical=canonical)
+                if t: t[3].record(stream)
                 comp_done[b].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(comp_done[b])
+                    if t: t[4].record(s_out)
                     for h_, d_ in zip(host_out[b], dout):
                         h_.copy_(d_, non_blocking=True)
+                    if t: t[5].record(s_out)
                     out_done[b].record(s_out)
 
         e2e_run(2)
@@ -381,7 +398,7 @@ def run_ours(args):
             dist.barrier()
         es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         es.record(s_in)
-        e2e_run(e2e_steps)
+        e2e_run(e2e_steps, tl)
         s_out.wait_stream(s_in)
         s_out.wait_stream(stream)
         ee.record(s_out)
@@ -389,16 +406,32 @@ def run_ours(args):
         if any(p.device_status() for p in plans):
             raise RuntimeError("device error during the end-to-end leg")
         e2e_ms = max_over_ranks(es.elapsed_time(ee) / e2e_steps, dist if ws > 1 else None, dev)
+        up = [t[0].elapsed_time(t[1]) for t in tl]
+        comp = [t[2].elapsed_time(t[3]) for t in tl]
+        down = [t[4].elapsed_time(t[5]) for t in tl]
+        # time during which an upload and a download of different steps ran at once
+        both = 0.0
+        for i in range(1, e2e_steps):
+            a0, a1 = es.elapsed_time(tl[i][0]), es.elapsed_time(tl[i][1])
+            b0, b1 = es.elapsed_time(tl[i - 1][4]), es.elapsed_time(tl[i - 1][5])
+            both += max(0.0, min(a1, b1) - max(a0, b0))
+        timeline = {"upload_ms": round(float(np.mean(up)), 3), "compute_ms": round(float(np.mean(comp)), 3),
+                    "download_ms": round(float(np.mean(down)), 3),
+                    "upload_gbs": round(h2d / (np.mean(up) * 1e-3) / 1e9, 1),
+                    "download_gbs": round(d2h / (np.mean(down) * 1e-3) / 1e9, 1),
+                    "upload_download_overlap_ms_per_step": round(both / max(1, e2e_steps - 1), 3)}
         e2e = {"value": round(whole_job_tflops(fl_step, e2e_ms, ws), 2), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": e2e_steps,
                "pipeline": "uploads, compute and downloads on three streams, two device buffer sets",
+               "timeline": timeline,
                "host_link_gbs": host_link_gbs(host_in[0], dev_sets[0][0], s_in)}
 
     peaks, peak_kind = load_peaks()
     traffic, traffic_note = None, "no ncu capture for this kernel source / workload"
     mt = MEASURED_TRAFFIC
-    if (kernel_sha1() == mt["kernel_sha1"] and wl.name == mt["workload"] and wl.heads == mt["heads"]
+    if (kernel_sha1() == mt["kernel_sha1"] and source_sha1("plan.cu") == mt["plan_sha1"]
+            and wl.name == mt["workload"] and wl.heads == mt["heads"]
             and not n_text and not args.packed):
         traffic = mt["bytes"]
         traffic_note = ("DRAM bytes of the regular-layout launch (ncu capture of the 8-head case scaled x3); "
