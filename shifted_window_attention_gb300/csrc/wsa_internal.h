@@ -28,8 +28,7 @@ struct WorkItem {
 
 // Host geometry of a layout (plan.cu): window size, window boxes
 // (t0,t1,h0,h1,w0,w1 per window, enumeration order) and the attention work
-// items of `rows` query rows: windows heaviest first, each window's items
-// together.
+// items of `rows` query rows in heaviest-first order.
 wsa_status window_size(int T, int H, int W, int nt, int nh, int nw, int max_temporal, int* wt, int* wh,
                        int* ww);
 void layout_boxes(int T, int H, int W, int wt, int wh, int ww, bool shifted, std::vector<int>* dims);
