@@ -250,8 +250,6 @@ def run_ours(args):
     trans_bytes = 2.0 * N * C * 2 + 2 * 4.0 * N  # read + write rows, two int32 table reads
 
     use_rope = args.rope >= 0
-    if use_rope and args.packed:
-        raise SystemExit("--rope is timed on canonical rows only")
     if use_rope:
         # rotated Q/K of the current layer (window-local positions of its layout)
         qk_rot = [(torch.empty_like(sets[0][0]), torch.empty_like(sets[0][1])) for _ in range(2)]
@@ -274,7 +272,7 @@ def run_ours(args):
             if e: e[4 * l].record(stream)
             if use_rope:
                 qr, kr = qk_rot[l % 2]
-                wsa.rope(p, q, k, q_out=qr, k_out=kr, text_len=args.rope)
+                wsa.rope(p, q, k, q_out=qr, k_out=kr, canonical=canonical, text_len=args.rope)
                 q, k = qr, kr
             if n_text:
                 qt, kt, vt = tsets[l % n_sets]
@@ -509,6 +507,7 @@ def run_ours(args):
             "traffic_note": "launch-bound parity workload; no ncu capture",
         },
         "e2e": e2e,
+        # per layer: attention (+ text reduction), RoPE pass(es)
         "gpu_launches": (((2 if n_text else 1) + (0 if not use_rope else 2 if n_text else 1)) * L + transitions)
                         * args.steps,
         "clocks": clk,
