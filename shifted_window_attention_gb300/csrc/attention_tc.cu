@@ -413,6 +413,11 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     }
   };
   const bool tma_lane = kTma && lw == 0 && lane == 0;
+  // Which of the latest ring fills came by TMA (bit i: fill ring_iter - 1 -
+  // i), and the latest Q fill when it did (unit iteration + 1, else 0).  A
+  // slot is refilled only after its previous fill was consumed, so after an
+  // error only the last kSlots fills and the last Q fill can still be landing.
+  uint32_t tma_bits = 0, tma_q = 0;
   // Both panels of the packed rows [row, row + 128) of `head` (TMA path only).
   auto tma_tile = [&](const CUtensorMap* map, uint32_t dst, int row, int head, uint32_t bar) {
     mbar_expect_tx(bar, kTileBytes);
@@ -426,6 +431,7 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
       if (!acquire(bar_at(sm, B_RING_EMPTY + slot), ((ring_iter / kSlots) & 1) ^ 1, E_LOAD_RING_EMPTY))
         return false;
       const uint32_t full = bar_at(sm, B_RING_FULL + slot);
+      if (kTma) tma_bits = (tma_bits << 1) | (tma_row >= 0 ? 1u : 0u);
       if (kTma && tma_row >= 0) {
         if (tma_lane) tma_tile(which ? &prm.tm_v : &prm.tm_k, sm.ring + slot * kTileBytes, tma_row, head, full);
       } else {
@@ -464,6 +470,7 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     if (!acquire(bar_at(sm, B_Q_EMPTY), (unit_iter & 1) ^ 1, E_LOAD_Q_EMPTY)) break;
     const uint32_t qfull = bar_at(sm, B_Q_FULL);
     const int qrow0 = tma_row_of(qt0, nv, off), qrow1 = has1 ? tma_row_of(qt0 + 1, nv, off) : -1;
+    if (kTma) tma_q = qrow0 >= 0 || qrow1 >= 0 ? unit_iter + 1 : 0;
     if (kTma && qrow0 >= 0) {
       if (tma_lane) tma_tile(&prm.tm_q, sm.q0, qrow0, head, qfull);
     } else {
@@ -488,12 +495,30 @@ __device__ __forceinline__ void loader_role(const TcParams& prm, const Smem& sm,
     ++unit_iter;
   }
   cp_async_wait_all();
-  // After a failed wait, TMA loads this lane issued may still be landing and
-  // their barrier phases may never complete: give them a bounded time (a
-  // tile lands in microseconds) before the CTA releases its shared memory.
+  // After a failed wait, TMA loads this lane issued may still be landing.
+  // Wait for the barrier phase of each fill that came by TMA (every lane
+  // arrived on it right after the load was issued, so it completes when the
+  // bytes have landed), bounded and regardless of the error word.  A phase
+  // that does not complete in time (another gather warp gave up before its
+  // arrival) leaves a fixed bounded wait as the last resort before the CTA
+  // releases its shared memory.
   if (tma_lane && *reinterpret_cast<volatile int*>(err) != 0) {
     const long long t0 = clock64();
-    while (clock64() - t0 < kTmaDrainCycles) __nanosleep(1000);
+    auto drained = [&](uint32_t bar, uint32_t parity) {
+      while (!mbar_try(bar, parity))
+        if (clock64() - t0 > kTmaDrainCycles) return false;
+      return true;
+    };
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      if (i >= static_cast<int>(ring_iter) || !((tma_bits >> i) & 1u)) continue;
+      const uint32_t f = ring_iter - 1 - i;
+      ok = drained(bar_at(sm, B_RING_FULL + f % kSlots), (f / kSlots) & 1) && ok;
+    }
+    if (tma_q != 0) ok = drained(bar_at(sm, B_Q_FULL), (tma_q - 1) & 1) && ok;
+    if (!ok)
+      while (clock64() - t0 < 2 * kTmaDrainCycles) __nanosleep(1000);
   }
 }
 

@@ -32,7 +32,8 @@ def _bf16_bits_to_f32(a):
 
 def _one_window_plan(n):
     # the window's rows, already gathered in packed order: one window [0, n)
-    return types.SimpleNamespace(offsets=np.array([0, n], dtype=np.int64), ids=np.arange(n, dtype=np.int64))
+    return types.SimpleNamespace(offsets=np.array([0, n], dtype=np.int64), ids=np.arange(n, dtype=np.int64),
+                                 num_windows=1, num_tokens=n)
 
 
 def _compare_window(task):
@@ -58,6 +59,23 @@ def _compare_window(task):
         ssr += float(np.sum(ref * ref))
         count += diff.size
     return win, worst, ssd, ssr, count, worst_head
+
+
+def _compare_text_window(task):
+    """Worker: the oracle's [video window, text] segment attention of one
+    window for every listed head; returns the video-row error sums (as
+    _compare_window) and the window's text output T_w [n_text, heads, d]."""
+    import oracle
+
+    win, q, k, v, o, qt, kt, vt, heads, scale = task
+    q, k, v, o, qt, kt, vt = (_bf16_bits_to_f32(x) for x in (q, k, v, o, qt, kt, vt))
+    n = q.shape[0]
+    plan = _one_window_plan(n)
+    ref, t_w = oracle.window_attention_text(q, k, v, qt, kt, vt, plan, scale=scale)  # one window: T_w itself
+    diff = o.astype(np.float64) - ref
+    worst_head = int(heads[int(np.argmax(np.abs(diff).max(axis=(0, 2))))]) if diff.size else -1
+    return (win, float(np.max(np.abs(diff))), float(np.sum(diff * diff)), float(np.sum(ref * ref)), diff.size,
+            worst_head, t_w)
 
 
 def pool():
@@ -139,3 +157,40 @@ def compare_layer(q, k, v, o, plan, windows=None, heads=None, canonical=True, sc
         count += c
     rel = float(np.sqrt(ssd / max(ssr, 1e-300)))
     return worst, rel, where, count
+
+
+def compare_text_layer(q, k, v, o, q_txt, k_txt, v_txt, o_txt, plan, scale=None):
+    """The [video window, replicated text] layer (oracle.window_attention_text)
+    compared in full: every video row of every window and head, and the text
+    output T = (sum over windows of T_w) / W.  bf16 CPU tensors; canonical
+    rows.  Returns ((video max_abs, rel_rms, worst (window, head)), (text
+    max_abs, rel_rms))."""
+    qb, kb, vb, ob = (_bits(t) for t in (q, k, v, o))
+    tb = tuple(_bits(t) for t in (q_txt, k_txt, v_txt))
+    heads = list(range(q.shape[1]))
+
+    def tasks():
+        for win in range(plan.num_windows):
+            a, b = int(plan.offsets[win]), int(plan.offsets[win + 1])
+            rows = plan.ids[a:b].astype(np.int64)
+            yield (win, qb[rows], kb[rows], vb[rows], ob[rows], *tb, heads, scale)
+
+    worst, where, ssd, ssr = 0.0, None, 0.0, 0.0
+    t_sum = None
+    results = pool().imap_unordered(_compare_text_window, tasks(), chunksize=1)
+    while True:
+        try:
+            win, m, d2, r2, _, h, t_w = results.next(timeout=_TASK_TIMEOUT_S)
+        except StopIteration:
+            break
+        if where is None or m > worst:
+            worst, where = m, (win, h)
+        ssd += d2
+        ssr += r2
+        t_sum = t_w if t_sum is None else t_sum + t_w
+    t_ref = t_sum / plan.num_windows
+    t_got = o_txt.float().numpy().astype(np.float64)
+    t_diff = t_got - t_ref
+    text = (float(np.max(np.abs(t_diff))), float(np.sqrt(np.sum(t_diff ** 2) / max(np.sum(t_ref ** 2), 1e-300))))
+    return (worst, float(np.sqrt(ssd / max(ssr, 1e-300))), where), text
+

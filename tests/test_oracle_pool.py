@@ -46,3 +46,21 @@ def test_pooled_comparison_finds_a_planted_error():
     assert max_abs > 0.2 and where == (5, 1)
     # a comparison that leaves that window out does not see it
     assert oracle_pool.compare_layer(q, k, v, o, p, windows=[4, 6])[0] < 0.02
+
+
+def test_pooled_text_comparison_equals_the_plain_computation():
+    # the text output is the mean over every window's text rows: the pooled
+    # per-window sums must reproduce the oracle's whole-layer result
+    w = wsa_inputs.custom(4, 9, 16, 2, 9, 16, heads=2, head_dim=128, name="tiny-bf16")
+    p = oracle.make_plan(*_grid(w), 1)
+    q, k, v = wsa_inputs.qkv(w)
+    qt, kt, vt = (wsa_inputs.randn((20, 2, 128), 77 + j).to(torch.bfloat16) for j in range(3))
+    ref, ref_t = oracle.window_attention_text(*(t.double().numpy() for t in (q, k, v, qt, kt, vt)), p)
+    o, ot = torch.from_numpy(ref).to(torch.bfloat16), torch.from_numpy(ref_t).to(torch.bfloat16)
+    (vmax, vrel, _), (tmax, trel) = oracle_pool.compare_text_layer(q, k, v, o, qt, kt, vt, ot, p)
+    assert np.isclose(vmax, errors(o.double().numpy(), ref)[0], rtol=0, atol=1e-12)
+    assert np.isclose(tmax, errors(ot.double().numpy(), ref_t)[0], rtol=0, atol=1e-12)
+    assert np.isclose(trel, errors(ot.double().numpy(), ref_t)[1], rtol=1e-9)
+    ot2 = ot.clone()
+    ot2[3, 1, 5] += 0.5
+    assert oracle_pool.compare_text_layer(q, k, v, o, qt, kt, vt, ot2, p)[1][0] > 0.4
