@@ -575,12 +575,11 @@ __device__ __forceinline__ void scheduler_role(const TcParams& prm, const Smem& 
 // wait for issue slots behind the two softmax warps of the sub-partition.
 // Measured: 1176 / 1090 TFLOP/s canonical and 1342 / 1235 packed at 720p
 // against 1165 / 1073 and 1317 / 1213 with the lone lane.
-// kStepDesc (the TMA instantiation): every descriptor is a step-0 descriptor
-// plus a constant, computed once per kernel (Q) or per tile (K, V), which
-// keeps the issue path between MMAs shorter.  Measured faster with TMA tiles
-// and slightly slower with the gather, so the gather instantiation keeps the
-// per-MMA descriptors.
-template <bool kText, bool kStepDesc>
+// Every descriptor is a step-0 descriptor plus a constant, computed once per
+// kernel (Q) or per tile (K, V), which keeps the issue path between MMAs
+// short (with the converged warp: 1196 / 1108 against 1169 / 1084 TFLOP/s
+// canonical at 720p, 1188 / 1171 against 1164 / 1140 at 1080p).
+template <bool kText>
 __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, uint32_t tmem) {
   int* err = prm.work + WS_ERROR;
   // every lane waits; the result is the same in all lanes
@@ -592,24 +591,14 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
   const uint64_t dQ0 = desc_kmajor(sm.q0, 0), dQ1 = desc_kmajor(sQ1, 0);
   uint32_t ring_iter = 0, unit_iter = 0, p_cnt0 = 0, p_cnt1 = 0;
   // S_t = Q_t K^T over the 8 K-steps of the key tile at kt
-  auto issue_s = [&](uint32_t tS, uint32_t sq, uint64_t dq, uint32_t kt, uint64_t dk) {
-    if constexpr (kStepDesc) {
+  auto issue_s = [&](uint32_t tS, uint64_t dq, uint64_t dk) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ss(tS, dq + kmajor_step(kk), dk + kmajor_step(kk), kIdescS, kk > 0);
-    } else {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ss(tS, desc_kmajor(sq, kk), desc_kmajor(kt, kk), kIdescS, kk > 0);
-    }
+    for (int kk = 0; kk < 8; ++kk) mma_ss(tS, dq + kmajor_step(kk), dk + kmajor_step(kk), kIdescS, kk > 0);
   };
   // O_t (+)= P_t V over the 8 K-steps of the value tile at vt
-  auto issue_pv = [&](uint32_t tO, uint32_t tP, uint32_t vt, uint64_t dv, bool acc_first) {
-    if constexpr (kStepDesc) {
+  auto issue_pv = [&](uint32_t tO, uint32_t tP, uint64_t dv, bool acc_first) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ts(tO, tP + 8 * kk, dv + v_step(kk), kIdescPV, (acc_first || kk > 0) ? 1u : 0u);
-    } else {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ts(tO, tP + 8 * kk, desc_v(vt, kk), kIdescPV, (acc_first || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 0; kk < 8; ++kk) mma_ts(tO, tP + 8 * kk, dv + v_step(kk), kIdescPV, (acc_first || kk > 0) ? 1u : 0u);
   };
   while (true) {
     const int us = unit_iter & 1;
@@ -620,7 +609,7 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
     const int nkv = (info.y + kTile - 1) / kTile + (kText ? (prm.n_text + kTile - 1) / kTile : 0);
     const bool has1 = q0 / kTile + 1 < nkv;
     bool ok = true;
-    uint32_t v_prev = 0, vslot_prev = 0;
+    uint32_t vslot_prev = 0;
     uint64_t dV_prev = 0;
     for (int j = 0; j < nkv; ++j) {
       const uint32_t kslot = ring_iter % kSlots;
@@ -631,7 +620,7 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
       if (elect_one()) {
         fence_proxy_async();  // rows landed by cp.async -> visible to the tensor core
         tc_fence_after();
-        issue_s(tS0, sm.q0, dQ0, kt, dK);
+        issue_s(tS0, dQ0, dK);
         tc_commit(bar_at(sm, B_S_FULL + 0));
       }
       __syncwarp();
@@ -643,12 +632,12 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
         if (j > 0) {
           if (has1) {
             tc_fence_after();
-            issue_pv(tO1, tS1, v_prev, dV_prev, j > 1);
+            issue_pv(tO1, tS1, dV_prev, j > 1);
           }
           tc_commit(bar_at(sm, B_RING_EMPTY + vslot_prev));
         }
         if (has1) {
-          issue_s(tS1, sQ1, dQ1, kt, dK);
+          issue_s(tS1, dQ1, dK);
           tc_commit(bar_at(sm, B_S_FULL + 1));
         }
         tc_commit(bar_at(sm, B_RING_EMPTY + kslot));
@@ -665,11 +654,10 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
       if (elect_one()) {
         fence_proxy_async();
         tc_fence_after();
-        issue_pv(tO0, tS0, vt, dV, j > 0);
+        issue_pv(tO0, tS0, dV, j > 0);
       }
       __syncwarp();
       ++ring_iter;
-      v_prev = vt;
       dV_prev = dV;
       vslot_prev = vslot;
     }
@@ -681,7 +669,7 @@ __device__ __forceinline__ void mma_role(const TcParams& prm, const Smem& sm, ui
     if (elect_one()) {
       if (has1) {
         tc_fence_after();
-        issue_pv(tO1, tS1, v_prev, dV_prev, nkv > 1);
+        issue_pv(tO1, tS1, dV_prev, nkv > 1);
       }
       tc_commit(bar_at(sm, B_RING_EMPTY + vslot_prev));
       tc_commit(bar_at(sm, B_O_FULL + 0));
@@ -955,7 +943,7 @@ __global__ void __maxnreg__(168) attention_tc_kernel(const __grid_constant__ TcP
   } else if (warp < kMmaWarp) {
     loader_role<kText, kTma>(prm, sm, warp - kLoaderWarp0, lane);
   } else if (warp == kMmaWarp) {
-    mma_role<kText, kTma>(prm, sm, tmem);
+    mma_role<kText>(prm, sm, tmem);
   } else if (lane == 0) {
     scheduler_role(prm, sm);
   }
