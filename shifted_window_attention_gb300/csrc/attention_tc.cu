@@ -710,6 +710,15 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a0, uint32_t a1, 
                : "memory");
 }
 
+// acc.x += lo(w), acc.y += hi(w) for the two bf16 halves of w, in fp32
+// (the conversion of a bf16 to fp32 is exact, so the sums are those of the
+// unpacked values).
+__device__ __forceinline__ void add_bf16x2_f32(float2& acc, uint32_t w) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -786,8 +795,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool firs
       // The row sum uses the bf16-rounded P that the P V product sees, so the
       // output is an exact convex combination of V rows up to fp32
       // accumulation (matters for peaked rows where |O| approaches |V|).
-      const float2 r = make_float2(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u));
-      if (i & 1) lb = __fadd2_rn(lb, r); else la = __fadd2_rn(la, r);
+      if (i & 1) add_bf16x2_f32(lb, pk[i]); else add_bf16x2_f32(la, pk[i]);
     }
     // P (bf16 pairs): S columns 64h..64h+63 become P columns 32h..32h+31.
     tmem_st32(tS + 32 * h, pk);
