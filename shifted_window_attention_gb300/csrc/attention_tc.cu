@@ -347,6 +347,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      WSA_W8(0), WSA_W8(8)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -730,11 +738,102 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // running sum l2 (two partial sums), rescales O in TMEM when the max grows by
 // more than kRescaleLog2 (log2), and writes the bf16 probabilities P over the first 64
 // columns of S.  kFull: all 128 key columns are valid (no masking).
-template <bool kFull>
+// A full key tile whose row max grew past the threshold in some row of the
+// warp: the max-first order (max, rescale of O and the sums, exponentials),
+// reading S in 32-column pieces.  Piece h's P lands in columns 16h..16h+15,
+// whose scores were read by then; the sums take the pairs in the same order.
+__device__ __forceinline__ void softmax_tile_redo(uint32_t tS, uint32_t tO, float c, float& m, float2& la,
+                                                  float2& lb) {
+  float mx = -INFINITY;
+#pragma unroll 1
+  for (int h = 0; h < 4; ++h) {
+    float y[32];
+    tmem_ld32(tS + 32 * h, y);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, y[i]);
+  }
+  const float m_new = fmaxf(m, mx * c);
+  const float alpha = ex2(m - m_new);
+  la = __fmul2_rn(la, make_float2(alpha, alpha));
+  lb = __fmul2_rn(lb, make_float2(alpha, alpha));
+  m = m_new;
+#pragma unroll 1
+  for (int h = 0; h < 4; ++h) {
+    float o[32];
+    tmem_ld32(tO + 32 * h, o);
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(o[i] * alpha);
+    tmem_st32(tO + 32 * h, r);
+  }
+  tmem_wait_st();
+  const float2 cc = make_float2(c, c);
+  const float2 nm = make_float2(-m, -m);
+#pragma unroll 1
+  for (int h = 0; h < 4; ++h) {
+    float y[32];
+    tmem_ld32(tS + 32 * h, y);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 a = __ffma2_rn(make_float2(y[2 * i], y[2 * i + 1]), cc, nm);
+      pk[i] = pack_bf16(ex2(a.x), ex2(a.y));
+      if (i & 1) add_bf16x2_f32(lb, pk[i]); else add_bf16x2_f32(la, pk[i]);
+    }
+    tmem_st16(tS + 16 * h, pk);
+  }
+}
+
+// kSpec (the TMA instantiation): full tiles after the first take the
+// exponentials of their first half at the current running max while the row
+// max is found alongside (below); the gather instantiation, where it measured
+// slower, finds the max first.
+template <bool kFull, bool kSpec>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool first, int kv_valid, float c,
                                              float& m, float2& la, float2& lb) {
   float x[128];
   tmem_ld128(tS, x);
+  if (kSpec && kFull && !first) {
+    // The running max moves only when a row max exceeds it by more than
+    // kRescaleLog2, so the first half's exponentials are taken with the
+    // current max while the row max is found alongside them, off the path
+    // from S to P.  When the check calls for a rescale (rare), nothing has
+    // been stored or summed yet, and the tile is redone from S (still intact
+    // in TMEM) in 32-column pieces, in the same order as the max-first path:
+    // the same bits, and few registers, so the common path keeps all of its.
+    const float2 cc = make_float2(c, c);
+    const float2 nm = make_float2(-m, -m);
+    uint32_t pk[32];
+    float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[64], x[65]);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = 2 * i;
+      if (i > 0) {
+        m0 = fmax3(m0, x[e], x[e + 1]);
+        m1 = fmax3(m1, x[64 + e], x[65 + e]);
+      }
+      const float2 a = __ffma2_rn(make_float2(x[e], x[e + 1]), cc, nm);
+      pk[i] = pack_bf16(ex2(a.x), ex2(a.y));
+    }
+    if (__any_sync(0xffffffffu, fmaxf(m0, m1) * c > m + kRescaleLog2)) {
+      softmax_tile_redo(tS, tO, c, m, la, lb);
+      return;
+    }
+    tmem_st32(tS, pk);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i & 1) add_bf16x2_f32(lb, pk[i]); else add_bf16x2_f32(la, pk[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = 64 + 2 * i;
+      const float2 a = __ffma2_rn(make_float2(x[e], x[e + 1]), cc, nm);
+      pk[i] = pack_bf16(ex2(a.x), ex2(a.y));
+      if (i & 1) add_bf16x2_f32(lb, pk[i]); else add_bf16x2_f32(la, pk[i]);
+    }
+    tmem_st32(tS + 32, pk);
+    return;
+  }
   float mx;
   if (kFull) {
     // columns 0-3 seed four chains, 4-123 take 15 rounds of 8, 124-127 close two chains
@@ -804,7 +903,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, bool firs
 
 // Softmax warps: warp w handles Q tile w/4, TMEM lanes 32*(w%4) .. +31; the
 // thread owns one query row.
-template <bool kText>
+template <bool kText, bool kSpec>
 __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm, uint32_t tmem, int warp,
                                              int lane) {
   int* err = prm.work + WS_ERROR;
@@ -837,9 +936,9 @@ __device__ __forceinline__ void softmax_role(const TcParams& prm, const Smem& sm
         const int kv_valid =
             !kText || j < nvt ? min(kTile, nv - j * kTile) : min(kTile, prm.n_text - (j - nvt) * kTile);
         if (kv_valid == kTile)
-          softmax_tile<true>(tS, tO, j == 0, kv_valid, c, m, la, lb);
+          softmax_tile<true, kSpec>(tS, tO, j == 0, kv_valid, c, m, la, lb);
         else
-          softmax_tile<false>(tS, tO, j == 0, kv_valid, c, m, la, lb);
+          softmax_tile<false, kSpec>(tS, tO, j == 0, kv_valid, c, m, la, lb);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_at(sm, B_P_FULL + t));
@@ -947,7 +1046,7 @@ __global__ void __maxnreg__(168) attention_tc_kernel(const __grid_constant__ TcP
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp < kLoaderWarp0) {
-    softmax_role<kText>(prm, sm, tmem, warp, lane);
+    softmax_role<kText, kTma>(prm, sm, tmem, warp, lane);
   } else if (warp < kMmaWarp) {
     loader_role<kText, kTma>(prm, sm, warp - kLoaderWarp0, lane);
   } else if (warp == kMmaWarp) {
