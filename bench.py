@@ -38,11 +38,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) of one regular-layout attention launch of the
 # 24-head 720p workload with canonical rows: an ncu capture of the same grid
-# with 8 heads measured 886.0 MB (732.3 MB read, 153.7 MB written), scaled x3
+# with 8 heads measured 886.1 MB (732.0 MB read, 154.1 MB written), scaled x3
 # (each head's rows are disjoint, so traffic grows with the head count).
 # Valid only for the kernel source and the work-list source (plan.cu, whose
 # item order decides which key/value tiles are re-read) it was measured on.
-MEASURED_TRAFFIC = {"kernel_sha1": "9a6a3f5fa6a392ff", "plan_sha1": "2664da1284cc650f", "workload": "720p",
+MEASURED_TRAFFIC = {"kernel_sha1": "b89dd017275ec489", "plan_sha1": "2664da1284cc650f", "workload": "720p",
                     "heads": 24, "bytes": 2.658e9}
 
 
